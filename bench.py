@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Bench of the single-query resident search (score + partial top-K + merge).
+
+Workload: N = 1,000,000 corpus rows, D = 1024, fp32, unit-norm Gaussian rows
+(seed 1), 1,000 unit-norm queries (seed 2), 10 planted near-duplicates per
+query (seed 3), inner product, K = 8 (headline) with K = 32 and K = 100 timed
+in their own regions. One step = one query: the fused scoring kernel and the
+merge kernel. The corpus (4.1 GB) is larger than L2, so no flush is needed.
+
+Prints one JSON line. ``value`` is the achieved corpus-read rate in GB/s over
+the K = 8 timed steps (algorithmic bytes N*D*4 per step / device time).
+
+--impl reference times the oracle (the CPU reference of this tier) on a
+bounded row sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "search p50 µs & achieved HBM GB/s (vs 8 TB/s) at N=1M D=1024 K=8/32/100"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("single-query resident search: N=1,000,000 x D=1024 fp32 unit-norm Gaussian corpus "
+            "(4.1 GB resident), 1,000 queries with 10 planted near-duplicates each, inner product, K=8")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--n", type=int, default=1_000_000)
+    ap.add_argument("--d", type=int, default=1024)
+    ap.add_argument("--queries", type=int, default=1000)
+    ap.add_argument("--extra-k", default="32,100")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-gate", action="store_true")
+    ap.add_argument("--schedule", type=int, default=None)
+    ap.add_argument("--ctas-per-sm", type=int, default=None)
+    ap.add_argument("--stage-bytes", type=int, default=None)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("score_select.cu", "rbf_device.cuh", "rbf_internal.h"):
+        with open(os.path.join(ROOT, "resident_brute_force_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the scoring kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "score_select_f32_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_workload(n, d, nq):
+    import workloads
+    c = workloads.unit_corpus(n, d, seed=1)
+    qs = workloads.unit_queries(nq, d, seed=2)
+    planted = workloads.plant_near_duplicates(c, qs, per_query=10, noise=0.05, seed=3)
+    return c, qs, planted
+
+
+def result_d2h_bytes(k: int) -> int:
+    a_off = 16
+    b_off = (a_off + 4 * k + 15) // 16 * 16
+    return b_off + 4 * k
+
+
+def cpu_oracle_rate(c, qs, k, budget_s=12.0, max_queries=20, row_sample=None):
+    """Time the oracle as it stands on this host. Returns (GB/s, cores, sample text, per-query seconds)."""
+    import oracle
+    o = oracle.get()
+    cores = o.num_threads()
+    corpus = c if row_sample is None else c[:row_sample]
+    n, d = corpus.shape
+    times = []
+    t_start = time.perf_counter()
+    j = 0
+    while j < max_queries and (time.perf_counter() - t_start) < budget_s:
+        t0 = time.perf_counter()
+        o.topk(corpus, qs[j % len(qs)], k)
+        times.append(time.perf_counter() - t0)
+        j += 1
+    total = sum(times)
+    rate = len(times) * n * d * 4 / total / 1e9
+    sample = (f"{len(times)} queries x {n} rows x D={d} (K={k}; double scoring + full sort of all rows), "
+              f"{total:.1f} s of CPU work")
+    return rate, cores, sample, total / len(times)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    n, d = args.n, args.d
+    import oracle
+    import workloads
+    rows = max(1, n // 64)   # bounded row sample per step
+    c = workloads.unit_corpus(rows, d, seed=1)
+    qs = workloads.unit_queries(max(1, min(args.queries, 64)), d, seed=2)
+    o = oracle.get()
+    for j in range(args.warmup):
+        o.topk(c, qs[j % len(qs)], 8)
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        o.topk(c, qs[j % len(qs)], 8)
+    dt = time.perf_counter() - t0
+    rate = args.steps * rows * d * 4 / dt / 1e9
+    sample = f"{rows} of the {n} rows per step (D={d}, K=8), {args.steps} steps"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n": n, "d": d, "k": 8, "l2": "host run"},
+        "cpu_baseline": {"value": round(rate, 3), "unit": "GB/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(rate, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def percentile(xs, p):
+    s = sorted(xs)
+    if not s:
+        return None
+    i = min(len(s) - 1, max(0, int(round(p / 100.0 * (len(s) - 1)))))
+    return s[i]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+
+    import resident_brute_force_gb300 as rbf
+    if rbf._build.is_stale():
+        rbf._build.build()
+
+    n, d, nq = args.n, args.d, args.queries
+    c, qs, planted = make_workload(n, d, nq)
+    stream = torch.cuda.Stream()
+    eng = rbf.Engine(n, d, 256, stream=stream)
+    if args.schedule is not None:
+        eng.set_option(rbf.RBF_OPT_SCHEDULE, args.schedule)
+    if args.ctas_per_sm is not None:
+        eng.set_option(rbf.RBF_OPT_CTAS_PER_SM, args.ctas_per_sm)
+    if args.stage_bytes is not None:
+        eng.set_option(rbf.RBF_OPT_STAGE_BYTES, args.stage_bytes)
+    eng.upload_corpus_rowmajor(c)
+    dq = torch.from_numpy(qs).cuda()
+    d_idx = torch.empty(256, dtype=torch.int32, device="cuda")
+    d_sc = torch.empty(256, dtype=torch.float32, device="cuda")
+
+    # Correctness gate before any timing: planted rows lead for a sample of
+    # queries, and one query matches the oracle under the parity rule.
+    if not args.no_gate:
+        for j in range(0, nq, max(1, nq // 20)):
+            idx, _ = eng.search_resident(qs[j], 32)
+            assert set(idx[:10].tolist()) == set(planted[j].tolist()), f"planted rows missing for query {j}"
+        if rank == 0:
+            import oracle
+            from tests.parity import check_float_topk
+            sigma = oracle.scores(c, qs[0])
+            for k in (8, 32, 100):
+                idx, sc = eng.search_resident(qs[0], k)
+                check_float_topk(idx, sc, sigma, k)
+
+    bytes_per_step = n * d * 4
+    ks = [8] + [int(x) for x in args.extra_k.split(",") if x]
+    sampler = ClockSampler(local)
+    per_k = {}
+    headline = None
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    sampler.start()
+    for k in ks:
+        with torch.cuda.stream(stream):
+            for j in range(args.warmup):
+                eng.search_resident_dev(dq[j % nq], k, d_idx, d_sc)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for j in range(args.steps):
+                e0, e1, e2 = evs[j]
+                e0.record(stream)
+                eng.score_select_partials_dev(dq[j % nq], k)
+                e1.record(stream)
+                eng.merge_partial_topk_dev(k, d_idx, d_sc)
+                e2.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        step_ms = [evs[j][0].elapsed_time(evs[j][2]) for j in range(args.steps)]
+        k1_ms = [evs[j][0].elapsed_time(evs[j][1]) for j in range(args.steps)]
+        total_ms = evs[0][0].elapsed_time(evs[-1][2])
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([total_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+        rec = {
+            "p50_us": round(percentile(step_ms, 50) * 1e3, 2),
+            "p99_us": round(percentile(step_ms, 99) * 1e3, 2),
+            "gbs": round(world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9, 1),
+            "qps": round(world * args.steps / (total_ms * 1e-3), 1),
+            "score_select_us_mean": round(statistics.mean(k1_ms) * 1e3, 2),
+            "merge_us_mean": round(statistics.mean(s - a for s, a in zip(step_ms, k1_ms)) * 1e3, 2),
+        }
+        per_k[str(k)] = rec
+        if k == 8:
+            headline = (total_ms, k1_ms, step_ms)
+    clocks = sampler.stop()
+
+    # End to end through the public host-buffer call: pinned staging of the
+    # query inside search_resident, H2D, kernels, D2H of the K results.
+    e2e = None
+    if not args.no_e2e:
+        for j in range(args.warmup):
+            eng.search_resident(qs[j % nq], 8)
+        barrier()
+        t0 = time.perf_counter()
+        for j in range(args.steps):
+            eng.search_resident(qs[j % nq], 8)
+        dt = time.perf_counter() - t0
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([dt], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": round(world * args.steps * bytes_per_step / dt / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": d * 4, "d2h_bytes_per_step": result_d2h_bytes(8),
+               "p50_us": None, "ms_per_step": round(dt / args.steps * 1e3, 4)}
+
+    total_ms, k1_ms, step_ms = headline
+    value = world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    k1_mean_s = statistics.mean(k1_ms) * 1e-3
+    achieved = bytes_per_step / k1_mean_s / 1e9
+    roofline = {"kernel": "score_select_f32", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(), "bytes_per_launch": bytes_per_step,
+                "vs_8tbs": round(achieved / 8000.0, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, cores, sample, _ = cpu_oracle_rate(c, qs, 8)
+        cpu = {"value": round(rate, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n": n, "d": d, "k": 8, "queries": nq,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (4.1 GB corpus), no flush"},
+            "p50_us": per_k["8"]["p50_us"], "p99_us": per_k["8"]["p99_us"], "per_k": per_k,
+            "k100_over_k8": round(per_k["100"]["p50_us"] / per_k["8"]["p50_us"], 3) if "100" in per_k else None,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,217 @@
+/*
+ * rbf.h -- C ABI of the GB300 resident brute-force top-K library (librbf.so).
+ *
+ * Exact top-K retrieval over a corpus that stays in GPU memory: a query of D
+ * floats is scored by inner product against N corpus rows, and the K rows
+ * with the highest scores come back best-first (GPU-Resident Top-K for
+ * Agentic RAG, section 2 and the "architecture mental model" pipeline:
+ * query up, score, per-block partial top-K, merge, K indices + K scores down).
+ *
+ * Ordering rule used by every entry point (same article, section 3, problem
+ * B): a higher score is better; on an exactly equal fp32 score the lower row
+ * index is better. -0.0 and +0.0 are equal; a NaN score ranks as -infinity.
+ * Results are always best-first.
+ *
+ * Conventions
+ *   - All sizes are element counts. Matrices are dense row-major.
+ *   - "host" pointers are ordinary CPU memory (pageable or pinned);
+ *     "device" pointers are CUDA device memory on the engine's device.
+ *   - The caller owns every pointer it passes; the library keeps none of them
+ *     after the call returns.
+ *   - The engine owns all device memory it uses. It is allocated in
+ *     rbf_create and nothing is allocated afterwards (the article's "engine
+ *     initialise" step, section 3 problem C and section 4 step 0).
+ *   - Calls ending in _dev are stream-ordered on the engine's stream: they
+ *     enqueue work and return; their outputs are valid once that stream has
+ *     reached them. The other calls are synchronous.
+ *   - Errors are returned, never thrown. On any error the caller's output
+ *     buffers are left untouched. RBF_ERR_CUDA records the CUDA error code,
+ *     readable with rbf_last_cuda_error.
+ *   - One engine is not safe for concurrent calls from several host threads;
+ *     callers serialise (the article's own caveat, section 9).
+ */
+#ifndef RBF_H_
+#define RBF_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct rbf_engine rbf_engine;
+
+typedef enum rbf_status {
+  RBF_OK = 0,
+  RBF_ERR_INVALID_VALUE = 1, /* bad size, K, pointer or flag */
+  RBF_ERR_NOT_READY = 2,     /* search before any corpus upload */
+  RBF_ERR_OUT_OF_MEMORY = 3, /* rbf_create could not allocate */
+  RBF_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  RBF_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+  RBF_ERR_UNSUPPORTED = 6    /* valid request this build does not handle */
+} rbf_status;
+
+/* Largest K any entry point accepts (the article's kMaxSupportedK,
+ * section 4 step 3). */
+#define RBF_MAX_K 256
+/* Largest embedding width D. */
+#define RBF_MAX_D 8192
+
+/* rbf_create flags. 0 means RBF_FLAG_FP32_CORPUS. */
+#define RBF_FLAG_FP32_CORPUS 0x1u /* keep the fp32 corpus: single-query path */
+#define RBF_FLAG_BF16_CORPUS 0x2u /* also keep a bf16 copy: batched path */
+
+/* Engine options for rbf_set_option (launch shape of the scoring kernel). */
+typedef enum rbf_option {
+  RBF_OPT_CTAS_PER_SM = 1,   /* persistent CTAs per SM, 1..4 (default 1) */
+  RBF_OPT_STAGE_BYTES = 2,   /* target bytes per pipeline stage (default 32768) */
+  RBF_OPT_SMEM_BUDGET = 3,   /* shared-memory ring budget per CTA, bytes */
+  RBF_OPT_TIMEOUT_NS = 4,    /* bound on every device-side wait (default 2e9) */
+  RBF_OPT_SCHEDULE = 5       /* 0 = static row ranges, 1 = dynamic tile claims */
+} rbf_option;
+
+/* ------------------------------------------------------------------ engine */
+
+/* Create an engine on the current CUDA device and allocate everything it will
+ * ever use, sized for the worst case (max_n rows, max_d columns, max_k results,
+ * max_batch queries per batched call).
+ *   max_n      1 .. 2^31-1
+ *   max_d      1 .. RBF_MAX_D
+ *   max_k      1 .. RBF_MAX_K
+ *   max_batch  1 .. 4096 (>= 1 even if only single queries are used)
+ *   flags      RBF_FLAG_* (0 = fp32 corpus only)
+ *   cuda_stream  a cudaStream_t to run on, or NULL for an engine-owned
+ *                non-blocking stream. A caller stream must outlive the engine.
+ *   out        receives the engine handle.
+ * Errors: INVALID_VALUE (a size out of range, out == NULL),
+ *         OUT_OF_MEMORY (device or pinned-host allocation failed),
+ *         CUDA (no usable device). */
+rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_batch,
+                      uint32_t flags, void* cuda_stream, rbf_engine** out);
+
+/* Synchronise the engine's stream and free everything it owns. NULL is a no-op. */
+rbf_status rbf_destroy(rbf_engine* engine);
+
+/* The cudaStream_t the engine runs on. */
+void* rbf_stream(const rbf_engine* engine);
+
+/* Number of SMs of the engine's device. */
+int32_t rbf_num_sms(const rbf_engine* engine);
+
+/* Number of per-CTA partial lists the scoring step writes for the resident
+ * corpus (0 before an upload). */
+int32_t rbf_num_partials(const rbf_engine* engine);
+
+/* Change a launch option (see rbf_option); takes effect on the next call. */
+rbf_status rbf_set_option(rbf_engine* engine, rbf_option option, int64_t value);
+
+/* Human-readable name of a status code (static string). */
+const char* rbf_status_string(rbf_status status);
+
+/* cudaError_t value of the most recent RBF_ERR_CUDA on this engine. */
+int32_t rbf_last_cuda_error(const rbf_engine* engine);
+
+/* Synchronise the stream and return (and clear) any error a device kernel
+ * recorded since the last check: RBF_ERR_TIMEOUT if a bounded wait ran out. */
+rbf_status rbf_check_device_error(rbf_engine* engine);
+
+/* ------------------------------------------------------------------ ingest */
+
+/* Copy a row-major N x D fp32 corpus into the engine and make it resident
+ * (the article's upload_corpus_rowmajor, section 4 step 1). corpus may be a
+ * host or a device pointer. Rows are stored with a pitch rounded up to a
+ * multiple of 4 floats and zero-padded; with RBF_FLAG_BF16_CORPUS a bf16 copy
+ * (round-to-nearest-even) is made too. A new upload replaces the old corpus.
+ * Blocks until the copy is complete.
+ * Errors: INVALID_VALUE (N < 1, N > max_n, D < 1, D > max_d, corpus NULL). */
+rbf_status upload_corpus_rowmajor(rbf_engine* engine, const float* corpus, int64_t n, int32_t d);
+
+/* ---------------------------------------------------------- single query */
+
+/* Top-K of one query against the resident corpus (the article's
+ * search_resident, section 4 steps 2-6): H2D of the D-float query, the fused
+ * score + per-CTA partial top-K kernel, the merge kernel, D2H of K indices and
+ * K scores.
+ *   query      host, D floats (D of the resident corpus)
+ *   k          1 .. min(max_k, N)
+ *   out_idx    host, K int32 row indices, best-first
+ *   out_score  host, K fp32 scores (fp32 accumulation of the inner product)
+ * Errors: INVALID_VALUE, NOT_READY, CUDA, TIMEOUT. */
+rbf_status search_resident(rbf_engine* engine, const float* query, int32_t k, int32_t* out_idx,
+                           float* out_score);
+
+/* As search_resident, with the query and outputs in device memory,
+ * stream-ordered. d_query needs no alignment beyond 4 bytes. */
+rbf_status search_resident_dev(rbf_engine* engine, const float* d_query, int32_t k, int32_t* d_idx,
+                               float* d_score);
+
+/* Step 1 of search_resident_dev alone: score every resident row against
+ * d_query and leave one best-first top-K list per CTA in the engine's
+ * workspace (the article's scoring and per-block partial top-K steps,
+ * section 4 steps 2-3, fused so the N scores never reach memory).
+ * Stream-ordered. */
+rbf_status score_select_partials_dev(rbf_engine* engine, const float* d_query, int32_t k);
+
+/* Step 2 of search_resident_dev alone: merge the per-CTA lists left by the
+ * last score_select_partials_dev into the global top-K (the article's merge
+ * step, section 4 step 4), same k. Stream-ordered; outputs in device memory. */
+rbf_status merge_partial_topk_dev(rbf_engine* engine, int32_t k, int32_t* d_idx, float* d_score);
+
+/* ---------------------------------------------------------------- batched */
+
+/* Top-K of each of B queries (row-major B x D) against the resident corpus.
+ * Needs RBF_FLAG_BF16_CORPUS: scores are bf16 x bf16 products (queries are
+ * rounded to bf16 on the device) accumulated in fp32 on the tensor cores.
+ *   queries    host, B x D floats
+ *   b          1 .. max_batch
+ *   k          1 .. min(max_k, N)
+ *   out_idx    host, B x K int32 (row q holds query q's list, best-first)
+ *   out_score  host, B x K fp32
+ * Errors: INVALID_VALUE, NOT_READY, UNSUPPORTED (no bf16 corpus), CUDA,
+ * TIMEOUT. */
+rbf_status search_resident_batch(rbf_engine* engine, const float* queries, int32_t b, int32_t k,
+                                 int32_t* out_idx, float* out_score);
+
+/* As search_resident_batch with device queries and outputs, stream-ordered. */
+rbf_status search_resident_batch_dev(rbf_engine* engine, const float* d_queries, int32_t b,
+                                     int32_t k, int32_t* d_idx, float* d_score);
+
+/* ---------------------------------------------------------- flat int32 */
+
+/* The K largest values of a flat int32 array in device memory, with their
+ * positions, largest first, lower position first among equal values
+ * (CUDA programming model series 9: stage 1 per-CTA top-K over a grid-stride
+ * share of the array, section 2; stage 2 one CTA over the GRID x K
+ * candidates, section 3.1).
+ *   d_data   device, n int32 (4-byte aligned; no other alignment needed)
+ *   n        1 .. 2^32-1
+ *   k        1 .. min(max_k, n)
+ *   out_val  host, K int32
+ *   out_pos  host, K int64
+ * Synchronous. Errors: INVALID_VALUE, CUDA, TIMEOUT. */
+rbf_status topk_int32(rbf_engine* engine, const int32_t* d_data, int64_t n, int32_t k,
+                      int32_t* out_val, int64_t* out_pos);
+
+/* As topk_int32 with device outputs, stream-ordered. */
+rbf_status topk_int32_dev(rbf_engine* engine, const int32_t* d_data, int64_t n, int32_t k,
+                          int32_t* d_val, int64_t* d_pos);
+
+/* ------------------------------------------------------------ self-test */
+
+/* Launch a one-block kernel that waits, with the engine's bounded-wait
+ * routine, on an mbarrier nothing ever arrives at, for at most timeout_ns.
+ * Returns RBF_ERR_TIMEOUT when the wait ran out and the kernel reported it
+ * (the expected outcome), RBF_OK if it somehow completed. The GPU context
+ * stays usable either way. */
+rbf_status rbf_selftest_wait_timeout(rbf_engine* engine, uint64_t timeout_ns);
+
+/* Host-side fault injection for tests: the next `count` CUDA operations of the
+ * given kind report failure without being issued. kind: 1 = copy, 2 = kernel
+ * launch. count 0 clears. Touches no GPU state. */
+rbf_status rbf_inject_host_fault(rbf_engine* engine, int32_t kind, int32_t count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RBF_H_ */

@@ -1,0 +1,260 @@
+"""ctypes binding of librbf.so (include/rbf.h), argument marshalling only.
+
+Every step of the search runs in the library's CUDA kernels. This module only
+turns numpy arrays / torch tensors into pointers and sizes, calls the C entry
+point of the same name, and raises ``RbfError`` on a non-zero status. If the
+library is missing it raises at once: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+RBF_OK = 0
+RBF_ERR_INVALID_VALUE = 1
+RBF_ERR_NOT_READY = 2
+RBF_ERR_OUT_OF_MEMORY = 3
+RBF_ERR_CUDA = 4
+RBF_ERR_TIMEOUT = 5
+RBF_ERR_UNSUPPORTED = 6
+
+RBF_MAX_K = 256
+RBF_MAX_D = 8192
+RBF_FLAG_FP32_CORPUS = 0x1
+RBF_FLAG_BF16_CORPUS = 0x2
+
+RBF_OPT_CTAS_PER_SM = 1
+RBF_OPT_STAGE_BYTES = 2
+RBF_OPT_SMEM_BUDGET = 3
+RBF_OPT_TIMEOUT_NS = 4
+RBF_OPT_SCHEDULE = 5
+
+FAULT_COPY = 1
+FAULT_LAUNCH = 2
+
+# Every symbol the header declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_U32 = ctypes.c_uint32
+_U64 = ctypes.c_uint64
+_S = ctypes.c_int
+SIGNATURES = {
+    "rbf_create": (_S, [_I64, _I32, _I32, _I32, _U32, _P, ctypes.POINTER(_P)]),
+    "rbf_destroy": (_S, [_P]),
+    "rbf_stream": (_P, [_P]),
+    "rbf_num_sms": (_I32, [_P]),
+    "rbf_num_partials": (_I32, [_P]),
+    "rbf_set_option": (_S, [_P, _S, _I64]),
+    "rbf_status_string": (ctypes.c_char_p, [_S]),
+    "rbf_last_cuda_error": (_I32, [_P]),
+    "rbf_check_device_error": (_S, [_P]),
+    "upload_corpus_rowmajor": (_S, [_P, _P, _I64, _I32]),
+    "search_resident": (_S, [_P, _P, _I32, _P, _P]),
+    "search_resident_dev": (_S, [_P, _P, _I32, _P, _P]),
+    "score_select_partials_dev": (_S, [_P, _P, _I32]),
+    "merge_partial_topk_dev": (_S, [_P, _I32, _P, _P]),
+    "search_resident_batch": (_S, [_P, _P, _I32, _I32, _P, _P]),
+    "search_resident_batch_dev": (_S, [_P, _P, _I32, _I32, _P, _P]),
+    "topk_int32": (_S, [_P, _P, _I64, _I32, _P, _P]),
+    "topk_int32_dev": (_S, [_P, _P, _I64, _I32, _P, _P]),
+    "rbf_selftest_wait_timeout": (_S, [_P, _U64]),
+    "rbf_inject_host_fault": (_S, [_P, _I32, _I32]),
+}
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load librbf.so. Raises if it has not been built."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    if _lib is None:
+        p = lib_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build() (nvcc, sm_103a)")
+        _lib = _declare(ctypes.CDLL(p))
+    return _lib
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+class RbfError(RuntimeError):
+    def __init__(self, status: int, where: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        name = load_library().rbf_status_string(status).decode()
+        extra = f" (cudaError {cuda_error})" if status == RBF_ERR_CUDA else ""
+        super().__init__(f"{where}: {name}{extra}")
+
+
+def status_string(status: int) -> str:
+    return load_library().rbf_status_string(status).decode()
+
+
+def _host_ptr(a: np.ndarray, dtype) -> tuple[np.ndarray, int]:
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+def _dev_ptr(t, dtype_name: str) -> int:
+    """Device pointer of a contiguous CUDA torch tensor of the given dtype."""
+    if not getattr(t, "is_cuda", False):
+        raise TypeError("expected a CUDA tensor")
+    if str(t.dtype) != f"torch.{dtype_name}":
+        raise TypeError(f"expected torch.{dtype_name}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _any_ptr(x, np_dtype, torch_dtype_name: str) -> tuple[object, int]:
+    """Pointer to host (numpy / CPU tensor) or device (CUDA tensor) data."""
+    if hasattr(x, "data_ptr"):
+        if x.is_cuda:
+            return x, _dev_ptr(x, torch_dtype_name)
+        x = x.numpy()
+    return _host_ptr(x, np_dtype)
+
+
+class Engine:
+    """An engine with every buffer preallocated (see ``rbf_create``)."""
+
+    def __init__(self, max_n: int, max_d: int, max_k: int = RBF_MAX_K, max_batch: int = 1,
+                 flags: int = 0, stream=None):
+        self.lib = load_library()
+        handle = ctypes.c_void_p()
+        s = None
+        if stream is not None:
+            s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        st = self.lib.rbf_create(int(max_n), int(max_d), int(max_k), int(max_batch), int(flags),
+                                 ctypes.c_void_p(s) if s else None, ctypes.byref(handle))
+        if st != RBF_OK:
+            raise RbfError(st, "rbf_create")
+        self._h = handle
+        self._stream_ref = stream
+        self.d = None
+        self.n = None
+
+    # -- lifetime
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self.lib.rbf_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _check(self, st: int, where: str) -> None:
+        if st != RBF_OK:
+            raise RbfError(st, where, self.lib.rbf_last_cuda_error(self._h))
+
+    # -- info / options
+    @property
+    def stream_handle(self) -> int:
+        return self.lib.rbf_stream(self._h) or 0
+
+    @property
+    def num_sms(self) -> int:
+        return self.lib.rbf_num_sms(self._h)
+
+    @property
+    def num_partials(self) -> int:
+        return self.lib.rbf_num_partials(self._h)
+
+    def last_cuda_error(self) -> int:
+        return self.lib.rbf_last_cuda_error(self._h)
+
+    def set_option(self, option: int, value: int) -> None:
+        self._check(self.lib.rbf_set_option(self._h, int(option), int(value)), "rbf_set_option")
+
+    def check_device_error(self) -> int:
+        return self.lib.rbf_check_device_error(self._h)
+
+    def selftest_wait_timeout(self, timeout_ns: int) -> int:
+        return self.lib.rbf_selftest_wait_timeout(self._h, int(timeout_ns))
+
+    def inject_host_fault(self, kind: int, count: int) -> None:
+        self._check(self.lib.rbf_inject_host_fault(self._h, int(kind), int(count)), "rbf_inject_host_fault")
+
+    # -- ingest
+    def upload_corpus_rowmajor(self, corpus) -> None:
+        keep, ptr = _any_ptr(corpus, np.float32, "float32")
+        n, d = corpus.shape
+        self._check(self.lib.upload_corpus_rowmajor(self._h, ptr, int(n), int(d)), "upload_corpus_rowmajor")
+        self.n, self.d = int(n), int(d)
+        del keep
+
+    # -- single query
+    def search_resident(self, query, k: int):
+        q, qp = _host_ptr(np.asarray(query).reshape(-1), np.float32)
+        idx = np.empty(max(int(k), 0), dtype=np.int32)
+        sc = np.empty(max(int(k), 0), dtype=np.float32)
+        self._check(self.lib.search_resident(self._h, qp, int(k), idx.ctypes.data, sc.ctypes.data),
+                    "search_resident")
+        return idx, sc
+
+    def search_resident_dev(self, d_query, k: int, d_idx, d_score) -> None:
+        self._check(self.lib.search_resident_dev(self._h, _dev_ptr(d_query, "float32"), int(k),
+                                                 _dev_ptr(d_idx, "int32"), _dev_ptr(d_score, "float32")),
+                    "search_resident_dev")
+
+    def score_select_partials_dev(self, d_query, k: int) -> None:
+        self._check(self.lib.score_select_partials_dev(self._h, _dev_ptr(d_query, "float32"), int(k)),
+                    "score_select_partials_dev")
+
+    def merge_partial_topk_dev(self, k: int, d_idx, d_score) -> None:
+        self._check(self.lib.merge_partial_topk_dev(self._h, int(k), _dev_ptr(d_idx, "int32"),
+                                                    _dev_ptr(d_score, "float32")), "merge_partial_topk_dev")
+
+    # -- batched
+    def search_resident_batch(self, queries, k: int):
+        q, qp = _host_ptr(np.asarray(queries), np.float32)
+        b = q.shape[0]
+        idx = np.empty((b, max(int(k), 0)), dtype=np.int32)
+        sc = np.empty((b, max(int(k), 0)), dtype=np.float32)
+        self._check(self.lib.search_resident_batch(self._h, qp, int(b), int(k), idx.ctypes.data,
+                                                   sc.ctypes.data), "search_resident_batch")
+        return idx, sc
+
+    def search_resident_batch_dev(self, d_queries, k: int, d_idx, d_score) -> None:
+        b = d_queries.shape[0]
+        self._check(self.lib.search_resident_batch_dev(self._h, _dev_ptr(d_queries, "float32"), int(b), int(k),
+                                                       _dev_ptr(d_idx, "int32"), _dev_ptr(d_score, "float32")),
+                    "search_resident_batch_dev")
+
+    # -- flat int32
+    def topk_int32(self, d_data, k: int):
+        val = np.empty(max(int(k), 0), dtype=np.int32)
+        pos = np.empty(max(int(k), 0), dtype=np.int64)
+        self._check(self.lib.topk_int32(self._h, _dev_ptr(d_data, "int32"), int(d_data.numel()), int(k),
+                                        val.ctypes.data, pos.ctypes.data), "topk_int32")
+        return val, pos
+
+    def topk_int32_dev(self, d_data, k: int, d_val, d_pos) -> None:
+        self._check(self.lib.topk_int32_dev(self._h, _dev_ptr(d_data, "int32"), int(d_data.numel()), int(k),
+                                            _dev_ptr(d_val, "int32"), _dev_ptr(d_pos, "int64")), "topk_int32_dev")

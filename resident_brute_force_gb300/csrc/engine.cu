@@ -1,0 +1,515 @@
+// engine.cu -- the engine behind the C ABI in include/rbf.h.
+//
+// The engine follows GPU-Resident Top-K for Agentic RAG (section 3 problem C
+// and section 4 steps 0-6): every device buffer is allocated once, sized for
+// the worst case, when the engine is created; the corpus is uploaded once and
+// stays resident; each query then costs one small host-to-device copy, the
+// kernels, and one small device-to-host copy of the K results. Here the
+// per-query kernels are the fused score + partial select kernel and the merge
+// kernel (score_select.cu, merge.cu); the flat int32 path is topk_i32.cu +
+// merge.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/rbf.h"
+#include "rbf_internal.h"
+
+using namespace rbf;
+
+namespace {
+
+constexpr int kMaxBatch = 4096;
+constexpr int kResultHeader = 16;  // error word + padding, ahead of the results
+constexpr int kMaxCtasPerSm = 4;
+constexpr int kI32CtasPerSm = 2;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct rbf_engine {
+  int device = 0;
+  int num_sms = 0;
+  int smem_optin = 0;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+
+  int64_t max_n = 0;
+  int max_d = 0, max_k = 0, max_batch = 0;
+  uint32_t flags = 0;
+  int max_pitch = 0;
+
+  // Resident corpus.
+  float* corpus = nullptr;
+  int64_t n = 0;
+  int d = 0;
+  int pitch = 0;
+  bool ready = false;
+
+  // Workspaces (device).
+  float* query = nullptr;        // max_batch * max_pitch floats
+  uint64_t* partials = nullptr;  // partials_cap keys
+  size_t partials_cap = 0;
+  int* errw = nullptr;           // [0] per call, [1] sticky, [2] self-test
+  unsigned* counters = nullptr;  // tile-claim counters of the dynamic schedule
+  uint8_t* result = nullptr;     // device result block
+  size_t result_bytes = 0;
+
+  // Pinned host staging.
+  uint8_t* h_query = nullptr;
+  uint8_t* h_result = nullptr;
+
+  // Options.
+  int ctas_per_sm = 1;
+  int stage_bytes = 32768;
+  int smem_budget = 0;  // 0: derived from the device limit
+  uint64_t timeout_ns = 2000000000ull;
+  int dynamic = 0;
+
+  // Last scoring launch (for merge_partial_topk_dev).
+  int last_lists = 0;
+  int last_k = 0;
+
+  int last_cuda_error = 0;
+  int fault_kind = 0;
+  int fault_count = 0;
+};
+
+namespace {
+
+rbf_status cuda_fail(rbf_engine* e, cudaError_t err) {
+  if (e) e->last_cuda_error = static_cast<int>(err);
+  return RBF_ERR_CUDA;
+}
+
+// Host-side fault injection: report a failure instead of issuing the next
+// operation of the armed kind.
+bool inject(rbf_engine* e, int kind) {
+  if (e->fault_count > 0 && e->fault_kind == kind) {
+    --e->fault_count;
+    e->last_cuda_error = static_cast<int>(cudaErrorUnknown);
+    return true;
+  }
+  return false;
+}
+
+#define RBF_COPY(e, call)                              \
+  do {                                                 \
+    if (inject((e), 1)) return RBF_ERR_CUDA;           \
+    cudaError_t _st = (call);                          \
+    if (_st != cudaSuccess) return cuda_fail((e), _st); \
+  } while (0)
+
+#define RBF_LAUNCH(e, call)                            \
+  do {                                                 \
+    if (inject((e), 2)) return RBF_ERR_CUDA;           \
+    cudaError_t _st = (call);                          \
+    if (_st != cudaSuccess) return cuda_fail((e), _st); \
+  } while (0)
+
+struct ScoreShape {
+  int rows_per_stage = 0;
+  int stages = 0;
+  int grid = 0;
+  int smem = 0;
+};
+
+// Launch shape of the fused scoring kernel for the resident corpus.
+bool score_shape(const rbf_engine* e, int k, ScoreShape* out) {
+  const int row_bytes = e->pitch * 4;
+  int budget = e->smem_budget;
+  if (budget <= 0) budget = std::min(e->smem_optin - 2048, 200 * 1024) / e->ctas_per_sm;
+  const int fixed = e->pitch * 4;  // query copy
+  for (int rps = std::max(1, e->stage_bytes / row_bytes); rps >= 1; rps = (rps > 1 ? rps / 2 : 0)) {
+    const int sb = rps * row_bytes;
+    int stages = (budget - fixed) / (sb + 32);
+    stages = std::min(stages, 32);
+    if (stages >= 2) {
+      const int smem = score_select_smem_bytes(e->pitch, k, rps, stages);
+      if (smem > e->smem_optin) continue;
+      out->rows_per_stage = rps;
+      out->stages = stages;
+      const int64_t tiles = (e->n + rps - 1) / rps;
+      out->grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, int64_t(e->num_sms) * e->ctas_per_sm)));
+      out->smem = smem;
+      return true;
+    }
+    if (rps == 1) break;
+  }
+  return false;
+}
+
+rbf_status check_k(const rbf_engine* e, int k) {
+  if (k < 1 || k > e->max_k || k > RBF_MAX_K || static_cast<int64_t>(k) > e->n) return RBF_ERR_INVALID_VALUE;
+  return RBF_OK;
+}
+
+rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k) {
+  ScoreShape sh;
+  if (!score_shape(e, k, &sh)) return RBF_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(sh.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+  ScoreSelectLaunch a;
+  a.corpus = e->corpus;
+  a.query = d_query;
+  a.partials = e->partials;
+  a.err = e->errw;
+  a.counters = e->counters;
+  a.n = e->n;
+  a.d = e->d;
+  a.pitch = e->pitch;
+  a.k = k;
+  a.rows_per_stage = sh.rows_per_stage;
+  a.stages = sh.stages;
+  a.stage_bytes = sh.rows_per_stage * e->pitch * 4;
+  a.grid = sh.grid;
+  a.dynamic = e->dynamic;
+  a.timeout_ns = e->timeout_ns;
+  RBF_LAUNCH(e, launch_score_select(a, e->stream));
+  e->last_lists = sh.grid;
+  e->last_k = k;
+  return RBF_OK;
+}
+
+rbf_status enqueue_merge(rbf_engine* e, int k, int lists, int queries, int int_keys, int32_t* out_a, void* out_b,
+                         int* result_err) {
+  MergeLaunch m;
+  m.partials = e->partials;
+  m.lists = lists;
+  m.queries = queries;
+  m.k = k;
+  m.int_keys = int_keys;
+  m.out_a = out_a;
+  m.out_b = out_b;
+  m.err_call = e->errw;
+  m.err_sticky = e->errw + 1;
+  m.result_err = result_err;
+  RBF_LAUNCH(e, launch_merge(m, e->stream));
+  return RBF_OK;
+}
+
+// Result block layout for `count` results: [err | pad][a: 4*count][b: eb*count]
+struct ResultLayout {
+  size_t a_off, b_off, bytes;
+};
+
+ResultLayout result_layout(size_t count, size_t eb) {
+  ResultLayout r;
+  r.a_off = kResultHeader;
+  r.b_off = align_up(r.a_off + 4 * count, 16);
+  r.bytes = r.b_off + eb * count;
+  return r;
+}
+
+rbf_status finish_host_call(rbf_engine* e, const ResultLayout& L) {
+  RBF_COPY(e, cudaMemcpyAsync(e->h_result, e->result, L.bytes, cudaMemcpyDeviceToHost, e->stream));
+  cudaError_t st = cudaStreamSynchronize(e->stream);
+  if (st != cudaSuccess) return cuda_fail(e, st);
+  int derr = 0;
+  std::memcpy(&derr, e->h_result, sizeof(int));
+  if (derr != 0) return RBF_ERR_TIMEOUT;
+  return RBF_OK;
+}
+
+void release(rbf_engine* e) {
+  if (!e) return;
+  if (e->stream) cudaStreamSynchronize(e->stream);
+  cudaFree(e->corpus);
+  cudaFree(e->query);
+  cudaFree(e->partials);
+  cudaFree(e->errw);
+  cudaFree(e->counters);
+  cudaFree(e->result);
+  cudaFreeHost(e->h_query);
+  cudaFreeHost(e->h_result);
+  if (e->own_stream && e->stream) cudaStreamDestroy(e->stream);
+  delete e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rbf_status_string(rbf_status s) {
+  switch (s) {
+    case RBF_OK: return "RBF_OK";
+    case RBF_ERR_INVALID_VALUE: return "RBF_ERR_INVALID_VALUE";
+    case RBF_ERR_NOT_READY: return "RBF_ERR_NOT_READY";
+    case RBF_ERR_OUT_OF_MEMORY: return "RBF_ERR_OUT_OF_MEMORY";
+    case RBF_ERR_CUDA: return "RBF_ERR_CUDA";
+    case RBF_ERR_TIMEOUT: return "RBF_ERR_TIMEOUT";
+    case RBF_ERR_UNSUPPORTED: return "RBF_ERR_UNSUPPORTED";
+  }
+  return "RBF_ERR_UNKNOWN";
+}
+
+rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_batch, uint32_t flags,
+                      void* cuda_stream, rbf_engine** out) {
+  if (!out) return RBF_ERR_INVALID_VALUE;
+  if (max_n < 1 || max_n > INT32_MAX || max_d < 1 || max_d > RBF_MAX_D || max_k < 1 || max_k > RBF_MAX_K ||
+      max_batch < 1 || max_batch > kMaxBatch)
+    return RBF_ERR_INVALID_VALUE;
+  if (flags & ~(RBF_FLAG_FP32_CORPUS | RBF_FLAG_BF16_CORPUS)) return RBF_ERR_INVALID_VALUE;
+  if (flags == 0) flags = RBF_FLAG_FP32_CORPUS;
+
+  rbf_engine* e = new (std::nothrow) rbf_engine();
+  if (!e) return RBF_ERR_OUT_OF_MEMORY;
+  cudaError_t st = cudaGetDevice(&e->device);
+  if (st != cudaSuccess) {
+    delete e;
+    return RBF_ERR_CUDA;
+  }
+  cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, e->device);
+  cudaDeviceGetAttribute(&e->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, e->device);
+  e->max_n = max_n;
+  e->max_d = max_d;
+  e->max_k = max_k;
+  e->max_batch = max_batch;
+  e->flags = flags;
+  e->max_pitch = static_cast<int>(align_up(static_cast<size_t>(max_d), 4));
+
+  if (cuda_stream) {
+    e->stream = static_cast<cudaStream_t>(cuda_stream);
+  } else {
+    st = cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking);
+    if (st != cudaSuccess) {
+      delete e;
+      return RBF_ERR_CUDA;
+    }
+    e->own_stream = true;
+  }
+
+  const size_t kpmax = static_cast<size_t>(list_width(max_k));
+  const size_t max_lists = static_cast<size_t>(e->num_sms) * kMaxCtasPerSm;
+  e->partials_cap = max_lists * kpmax;
+  const size_t result_count = static_cast<size_t>(max_batch) * max_k;
+  e->result_bytes = result_layout(result_count, 8).bytes;
+
+  bool ok = true;
+  if (flags & RBF_FLAG_FP32_CORPUS)
+    ok = ok && cudaMalloc(&e->corpus, static_cast<size_t>(max_n) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->counters, 4 * sizeof(unsigned)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->result, e->result_bytes) == cudaSuccess;
+  ok = ok && cudaMallocHost(&e->h_query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMallocHost(&e->h_result, e->result_bytes) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    release(e);
+    return RBF_ERR_OUT_OF_MEMORY;
+  }
+  ok = cudaMemsetAsync(e->errw, 0, 4 * sizeof(int), e->stream) == cudaSuccess &&
+       cudaMemsetAsync(e->counters, 0, 4 * sizeof(unsigned), e->stream) == cudaSuccess &&
+       cudaMemsetAsync(e->query, 0, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float), e->stream) ==
+           cudaSuccess &&
+       cudaStreamSynchronize(e->stream) == cudaSuccess;
+  if (!ok) {
+    release(e);
+    return RBF_ERR_CUDA;
+  }
+  *out = e;
+  return RBF_OK;
+}
+
+rbf_status rbf_destroy(rbf_engine* e) {
+  release(e);
+  return RBF_OK;
+}
+
+void* rbf_stream(const rbf_engine* e) { return e ? static_cast<void*>(e->stream) : nullptr; }
+
+int32_t rbf_num_sms(const rbf_engine* e) { return e ? e->num_sms : 0; }
+
+int32_t rbf_num_partials(const rbf_engine* e) {
+  if (!e || !e->ready) return 0;
+  ScoreShape sh;
+  return score_shape(e, 1, &sh) ? sh.grid : 0;
+}
+
+int32_t rbf_last_cuda_error(const rbf_engine* e) { return e ? e->last_cuda_error : 0; }
+
+rbf_status rbf_set_option(rbf_engine* e, rbf_option opt, int64_t value) {
+  if (!e) return RBF_ERR_INVALID_VALUE;
+  switch (opt) {
+    case RBF_OPT_CTAS_PER_SM:
+      if (value < 1 || value > kMaxCtasPerSm) return RBF_ERR_INVALID_VALUE;
+      e->ctas_per_sm = static_cast<int>(value);
+      return RBF_OK;
+    case RBF_OPT_STAGE_BYTES:
+      if (value < 16 || value > (1 << 20)) return RBF_ERR_INVALID_VALUE;
+      e->stage_bytes = static_cast<int>(value);
+      return RBF_OK;
+    case RBF_OPT_SMEM_BUDGET:
+      if (value < 0 || value > e->smem_optin) return RBF_ERR_INVALID_VALUE;
+      e->smem_budget = static_cast<int>(value);
+      return RBF_OK;
+    case RBF_OPT_TIMEOUT_NS:
+      if (value < 1000) return RBF_ERR_INVALID_VALUE;
+      e->timeout_ns = static_cast<uint64_t>(value);
+      return RBF_OK;
+    case RBF_OPT_SCHEDULE:
+      if (value != 0 && value != 1) return RBF_ERR_INVALID_VALUE;
+      e->dynamic = static_cast<int>(value);
+      return RBF_OK;
+  }
+  return RBF_ERR_INVALID_VALUE;
+}
+
+rbf_status rbf_check_device_error(rbf_engine* e) {
+  if (!e) return RBF_ERR_INVALID_VALUE;
+  int w = 0;
+  cudaError_t st = cudaStreamSynchronize(e->stream);
+  if (st == cudaSuccess) st = cudaMemcpyAsync(&w, e->errw + 1, sizeof(int), cudaMemcpyDeviceToHost, e->stream);
+  if (st == cudaSuccess) st = cudaMemsetAsync(e->errw + 1, 0, sizeof(int), e->stream);
+  if (st == cudaSuccess) st = cudaStreamSynchronize(e->stream);
+  if (st != cudaSuccess) return cuda_fail(e, st);
+  return w ? RBF_ERR_TIMEOUT : RBF_OK;
+}
+
+rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n, int32_t d) {
+  if (!e || !corpus || n < 1 || n > e->max_n || d < 1 || d > e->max_d) return RBF_ERR_INVALID_VALUE;
+  if (!e->corpus) return RBF_ERR_UNSUPPORTED;
+  e->ready = false;
+  const int pitch = static_cast<int>(align_up(static_cast<size_t>(d), 4));
+  RBF_COPY(e, cudaMemcpy2DAsync(e->corpus, static_cast<size_t>(pitch) * 4, corpus, static_cast<size_t>(d) * 4,
+                                static_cast<size_t>(d) * 4, static_cast<size_t>(n), cudaMemcpyDefault, e->stream));
+  if (pitch > d) {
+    RBF_COPY(e, cudaMemset2DAsync(e->corpus + d, static_cast<size_t>(pitch) * 4, 0,
+                                  static_cast<size_t>(pitch - d) * 4, static_cast<size_t>(n), e->stream));
+  }
+  cudaError_t st = cudaStreamSynchronize(e->stream);
+  if (st != cudaSuccess) return cuda_fail(e, st);
+  e->n = n;
+  e->d = d;
+  e->pitch = pitch;
+  e->ready = true;
+  e->last_lists = 0;
+  e->last_k = 0;
+  return RBF_OK;
+}
+
+rbf_status score_select_partials_dev(rbf_engine* e, const float* d_query, int32_t k) {
+  if (!e || !d_query) return RBF_ERR_INVALID_VALUE;
+  if (!e->ready) return RBF_ERR_NOT_READY;
+  if (rbf_status s = check_k(e, k)) return s;
+  return enqueue_score(e, d_query, k);
+}
+
+rbf_status merge_partial_topk_dev(rbf_engine* e, int32_t k, int32_t* d_idx, float* d_score) {
+  if (!e || !d_idx || !d_score) return RBF_ERR_INVALID_VALUE;
+  if (!e->ready || e->last_lists == 0) return RBF_ERR_NOT_READY;
+  if (k != e->last_k) return RBF_ERR_INVALID_VALUE;
+  return enqueue_merge(e, k, e->last_lists, 1, 0, d_idx, d_score, reinterpret_cast<int*>(e->result));
+}
+
+rbf_status search_resident_dev(rbf_engine* e, const float* d_query, int32_t k, int32_t* d_idx, float* d_score) {
+  if (!e || !d_query || !d_idx || !d_score) return RBF_ERR_INVALID_VALUE;
+  if (!e->ready) return RBF_ERR_NOT_READY;
+  if (rbf_status s = check_k(e, k)) return s;
+  if (rbf_status s = enqueue_score(e, d_query, k)) return s;
+  return enqueue_merge(e, k, e->last_lists, 1, 0, d_idx, d_score, reinterpret_cast<int*>(e->result));
+}
+
+rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t* out_idx, float* out_score) {
+  if (!e || !query || !out_idx || !out_score) return RBF_ERR_INVALID_VALUE;
+  if (!e->ready) return RBF_ERR_NOT_READY;
+  if (rbf_status s = check_k(e, k)) return s;
+  const size_t qbytes = static_cast<size_t>(e->d) * 4;
+  std::memcpy(e->h_query, query, qbytes);
+  RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
+  if (rbf_status s = enqueue_score(e, e->query, k)) return s;
+  const ResultLayout L = result_layout(static_cast<size_t>(k), 4);
+  if (rbf_status s = enqueue_merge(e, k, e->last_lists, 1, 0, reinterpret_cast<int32_t*>(e->result + L.a_off),
+                                   e->result + L.b_off, reinterpret_cast<int*>(e->result)))
+    return s;
+  if (rbf_status s = finish_host_call(e, L)) return s;
+  std::memcpy(out_idx, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
+  std::memcpy(out_score, e->h_result + L.b_off, 4 * static_cast<size_t>(k));
+  return RBF_OK;
+}
+
+rbf_status search_resident_batch_dev(rbf_engine* e, const float* d_queries, int32_t b, int32_t k, int32_t* d_idx,
+                                     float* d_score) {
+  if (!e || !d_queries || !d_idx || !d_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
+  if (!e->ready) return RBF_ERR_NOT_READY;
+  if (rbf_status s = check_k(e, k)) return s;
+  return RBF_ERR_UNSUPPORTED;
+}
+
+rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b, int32_t k, int32_t* out_idx,
+                                 float* out_score) {
+  if (!e || !queries || !out_idx || !out_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
+  if (!e->ready) return RBF_ERR_NOT_READY;
+  if (rbf_status s = check_k(e, k)) return s;
+  return RBF_ERR_UNSUPPORTED;
+}
+
+static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* val,
+                                     int64_t* pos, int* result_err) {
+  const int64_t per_cta = 8192;  // below this many elements per CTA, use fewer CTAs
+  int64_t grid = std::min<int64_t>(int64_t(e->num_sms) * kI32CtasPerSm, (n + per_cta - 1) / per_cta);
+  grid = std::max<int64_t>(grid, 1);
+  if (static_cast<size_t>(grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+  I32Launch a;
+  a.data = d_data;
+  a.n = n;
+  a.k = k;
+  a.partials = e->partials;
+  a.grid = static_cast<int>(grid);
+  RBF_LAUNCH(e, launch_topk_i32_stage1(a, e->stream));
+  return enqueue_merge(e, k, static_cast<int>(grid), 1, 1, val, pos, result_err);
+}
+
+static rbf_status check_i32_args(const rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k) {
+  if (!e || !d_data || n < 1 || n > int64_t(0xFFFFFFFFll)) return RBF_ERR_INVALID_VALUE;
+  if (k < 1 || k > e->max_k || static_cast<int64_t>(k) > n) return RBF_ERR_INVALID_VALUE;
+  if ((reinterpret_cast<uintptr_t>(d_data) & 3u) != 0) return RBF_ERR_INVALID_VALUE;
+  return RBF_OK;
+}
+
+rbf_status topk_int32_dev(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* d_val,
+                          int64_t* d_pos) {
+  if (rbf_status s = check_i32_args(e, d_data, n, k)) return s;
+  if (!d_val || !d_pos) return RBF_ERR_INVALID_VALUE;
+  return enqueue_topk_int32(e, d_data, n, k, d_val, d_pos, reinterpret_cast<int*>(e->result));
+}
+
+rbf_status topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* out_val,
+                      int64_t* out_pos) {
+  if (rbf_status s = check_i32_args(e, d_data, n, k)) return s;
+  if (!out_val || !out_pos) return RBF_ERR_INVALID_VALUE;
+  const ResultLayout L = result_layout(static_cast<size_t>(k), 8);
+  if (rbf_status s = enqueue_topk_int32(e, d_data, n, k, reinterpret_cast<int32_t*>(e->result + L.a_off),
+                                        reinterpret_cast<int64_t*>(e->result + L.b_off),
+                                        reinterpret_cast<int*>(e->result)))
+    return s;
+  if (rbf_status s = finish_host_call(e, L)) return s;
+  std::memcpy(out_val, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
+  std::memcpy(out_pos, e->h_result + L.b_off, 8 * static_cast<size_t>(k));
+  return RBF_OK;
+}
+
+rbf_status rbf_selftest_wait_timeout(rbf_engine* e, uint64_t timeout_ns) {
+  if (!e || timeout_ns < 1000 || timeout_ns > 10000000000ull) return RBF_ERR_INVALID_VALUE;
+  RBF_COPY(e, cudaMemsetAsync(e->errw + 2, 0, sizeof(int), e->stream));
+  RBF_LAUNCH(e, launch_wait_probe(e->errw + 2, timeout_ns, e->stream));
+  int w = 0;
+  RBF_COPY(e, cudaMemcpyAsync(&w, e->errw + 2, sizeof(int), cudaMemcpyDeviceToHost, e->stream));
+  cudaError_t st = cudaStreamSynchronize(e->stream);
+  if (st != cudaSuccess) return cuda_fail(e, st);
+  return w ? RBF_ERR_TIMEOUT : RBF_OK;
+}
+
+rbf_status rbf_inject_host_fault(rbf_engine* e, int32_t kind, int32_t count) {
+  if (!e || count < 0 || (count > 0 && kind != 1 && kind != 2)) return RBF_ERR_INVALID_VALUE;
+  e->fault_kind = kind;
+  e->fault_count = count;
+  return RBF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// rbf_internal.h -- host-side launch interfaces between the library's
+// translation units. Not part of the public ABI (that is include/rbf.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rbf {
+
+// Consumer warps of the fused scoring kernel (plus one producer warp).
+constexpr int kScoreConsumerWarps = 8;
+// Warps of the int32 stage-1 kernel.
+constexpr int kI32Warps = 16;
+
+// Candidate-list width for a K: the smallest power of two >= max(K, 32).
+inline int list_width(int k) {
+  int kp = 32;
+  while (kp < k) kp <<= 1;
+  return kp;
+}
+
+struct ScoreSelectLaunch {
+  const float* corpus;     // device, n rows of `pitch` floats, zero-padded past d
+  const float* query;      // device, d floats
+  uint64_t* partials;      // device, grid lists of list_width(k) keys
+  int* err;                // device error word (bits ORed in)
+  unsigned* counters;      // device, 2 words, zero between launches (dynamic schedule)
+  int64_t n;
+  int d;
+  int pitch;               // floats per stored row, multiple of 4
+  int k;
+  int rows_per_stage;
+  int stages;
+  int stage_bytes;
+  int grid;
+  int dynamic;             // 0 = static contiguous row ranges, 1 = tile claims
+  uint64_t timeout_ns;
+};
+
+// Shared memory the fused kernel needs for a launch shape.
+int score_select_smem_bytes(int pitch, int k, int rows_per_stage, int stages);
+cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream);
+
+struct MergeLaunch {
+  const uint64_t* partials;  // device, queries x lists x list_width(k) keys
+  int lists;                 // lists per query
+  int queries;               // one CTA per query
+  int k;
+  int int_keys;              // 0: (fp32 score, int32 index) keys; 1: (int32 value, position) keys
+  int32_t* out_a;            // float path: indices [queries x k]; int path: values [k]
+  void* out_b;               // float path: float scores; int path: int64 positions
+  int* err_call;             // per-call error word, moved out and cleared
+  int* err_sticky;           // sticky error word (ORed)
+  int* result_err;           // where the per-call error lands (may be null)
+};
+cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
+
+struct I32Launch {
+  const int32_t* data;
+  int64_t n;
+  int k;
+  uint64_t* partials;        // grid lists of list_width(k) keys
+  int grid;
+};
+cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
+
+cudaError_t launch_wait_probe(int* err, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace rbf
