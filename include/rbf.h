@@ -196,6 +196,37 @@ rbf_status topk_int32(rbf_engine* engine, const int32_t* d_data, int64_t n, int3
 rbf_status topk_int32_dev(rbf_engine* engine, const int32_t* d_data, int64_t n, int32_t k,
                           int32_t* d_val, int64_t* d_pos);
 
+/* No-allocation variant of topk_int32_dev, for callers that may not call
+ * cudaMalloc: for example a plugin inside an inference server or database
+ * whose GPU memory all comes from the host application's allocator (a
+ * cudaMalloc behind its back breaks that accounting and can synchronise the
+ * device, stalling the application's other streams), or latency-critical
+ * code that cannot wait for an allocation. The retrieval pages have no
+ * counterpart to this entry point.
+ *
+ * Needs no engine. It runs the same two kernels as topk_int32_dev with the
+ * same result; their scratch (one 256-key list per stage-1 CTA, at most 512
+ * lists) is a fixed 1 MiB array in the library's own device memory, which
+ * every GPU that loads the library keeps until the process exits. Nothing is
+ * allocated or freed, here or by any library routine it calls.
+ *   d_data    device, n int32 (4-byte aligned), on the current device
+ *   n         1 .. 2^32-1
+ *   k         1 .. min(RBF_MAX_K, n); a larger k is rejected with
+ *             RBF_ERR_INVALID_VALUE (the scratch lists hold 256 keys)
+ *   d_val     device, K int32, largest first
+ *   d_pos     device, K int64 positions
+ *   cuda_stream  stream to enqueue on (NULL = legacy default stream)
+ * Stream-ordered; returns once both kernels are enqueued.
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture. Every call shares the one array and it keeps the previous
+ * call's contents; each call writes every list it reads, so nothing needs
+ * clearing, but calls whose kernels overlap on the GPU (two streams, or two
+ * host threads) race on the array: serialise them.
+ * Errors: INVALID_VALUE (arguments), CUDA (lookup or launch failed). */
+rbf_status topk_int32_noalloc(const int32_t* d_data, int64_t n, int32_t k, int32_t* d_val, int64_t* d_pos,
+                              void* cuda_stream);
+
 /* ------------------------------------------------------------ self-test */
 
 /* Launch a one-block kernel that waits, with the engine's bounded-wait

@@ -6,6 +6,7 @@ only for device memory and streams.
 """
 from ._binding import (  # noqa: F401
     Engine,
+    topk_int32_noalloc,
     RbfError,
     load_library,
     lib_path,

@@ -62,6 +62,7 @@ SIGNATURES = {
     "search_resident_batch_dev": (_S, [_P, _P, _I32, _I32, _P, _P]),
     "topk_int32": (_S, [_P, _P, _I64, _I32, _P, _P]),
     "topk_int32_dev": (_S, [_P, _P, _I64, _I32, _P, _P]),
+    "topk_int32_noalloc": (_S, [_P, _I64, _I32, _P, _P, _P]),
     "rbf_selftest_wait_timeout": (_S, [_P, _U64]),
     "rbf_inject_host_fault": (_S, [_P, _I32, _I32]),
 }
@@ -92,6 +93,17 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         f.restype = res
         f.argtypes = args
     return lib
+
+
+def topk_int32_noalloc(d_data, k: int, d_val, d_pos, stream=None) -> int:
+    """Call topk_int32_noalloc (no engine, no device allocation); returns the
+    status code. All tensors are CUDA tensors on the current device."""
+    s = None
+    if stream is not None:
+        s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return load_library().topk_int32_noalloc(_dev_ptr(d_data, "int32"), int(d_data.numel()), int(k),
+                                             _dev_ptr(d_val, "int32"), _dev_ptr(d_pos, "int64"),
+                                             ctypes.c_void_p(s) if s else None)
 
 
 class RbfError(RuntimeError):
