@@ -30,6 +30,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "search p50 µs & achieved HBM GB/s (vs 8 TB/s) at N=1M D=1024 K=8/32/100"
 FALLBACK_HBM_GBS = 6800.0
+K1_SAMPLE = 8  # time the scoring kernel alone on every 8th step
 WORKLOAD = ("single-query resident search: N=1,000,000 x D=1024 fp32 unit-norm Gaussian corpus "
             "(4.1 GB resident), 1,000 queries with 10 planted near-duplicates each, inner product, K=8")
 
@@ -80,15 +81,22 @@ def kernel_source_hash() -> str:
 def ncu_traffic():
     """DRAM bytes per launch of the scoring kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "score_select_f32_traffic.json")
+    p = os.path.join(ROOT, "profiles", "score_select_f32_N100k_D1024_K8_ncu.md")
+    rec = {}
     try:
         with open(p) as f:
-            rec = json.load(f)
-    except Exception:
+            for line in f:
+                if ":" in line and not line.startswith(("|", "#", " ")):
+                    key, _, val = line.partition(":")
+                    rec[key.strip()] = val.strip()
+    except OSError:
         return None
     if rec.get("source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch_full_size")
+    try:
+        return int(rec["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
@@ -156,7 +164,7 @@ def result_d2h_bytes(k: int) -> int:
     return b_off + 4 * k
 
 
-def cpu_oracle_rate(c, qs, k, budget_s=12.0, max_queries=20, row_sample=None):
+def cpu_oracle_rate(c, qs, k, budget_s=12.0, max_queries=200, row_sample=None):
     """Time the oracle as it stands on this host. Returns (GB/s, cores, sample text, per-query seconds)."""
     import oracle
     o = oracle.get()
@@ -282,22 +290,26 @@ def main():
         with torch.cuda.stream(stream):
             for j in range(args.warmup):
                 eng.search_resident_dev(dq[j % nq], k, d_idx, d_sc)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        # Events at every step boundary; on every SAMPLE-th step one more
+        # event between the two kernels times the scoring kernel alone (an
+        # event there costs the merge its early launch, so only a sample).
+        bounds = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        mids = {j: torch.cuda.Event(enable_timing=True) for j in range(0, args.steps, K1_SAMPLE)}
         barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for j in range(args.steps):
-                e0, e1, e2 = evs[j]
-                e0.record(stream)
+                bounds[j].record(stream)
                 eng.score_select_partials_dev(dq[j % nq], k)
-                e1.record(stream)
+                if j in mids:
+                    mids[j].record(stream)
                 eng.merge_partial_topk_dev(k, d_idx, d_sc)
-                e2.record(stream)
+            bounds[args.steps].record(stream)
         torch.cuda.synchronize()
         barrier()
-        step_ms = [evs[j][0].elapsed_time(evs[j][2]) for j in range(args.steps)]
-        k1_ms = [evs[j][0].elapsed_time(evs[j][1]) for j in range(args.steps)]
-        total_ms = evs[0][0].elapsed_time(evs[-1][2])
+        step_ms = [bounds[j].elapsed_time(bounds[j + 1]) for j in range(args.steps)]
+        k1_ms = [bounds[j].elapsed_time(mids[j]) for j in sorted(mids)]
+        total_ms = bounds[0].elapsed_time(bounds[args.steps])
         if world > 1:
             import torch.distributed as dist
             t = torch.tensor([total_ms], device="cuda")
@@ -309,7 +321,8 @@ def main():
             "gbs": round(world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9, 1),
             "qps": round(world * args.steps / (total_ms * 1e-3), 1),
             "score_select_us_mean": round(statistics.mean(k1_ms) * 1e3, 2),
-            "merge_us_mean": round(statistics.mean(s - a for s, a in zip(step_ms, k1_ms)) * 1e3, 2),
+            "score_select_launches_timed": len(k1_ms),
+            "merge_and_gap_us_mean": round((statistics.mean(step_ms) - statistics.mean(k1_ms)) * 1e3, 2),
         }
         per_k[str(k)] = rec
         if k == 8:
@@ -323,9 +336,12 @@ def main():
         for j in range(args.warmup):
             eng.search_resident(qs[j % nq], 8)
         barrier()
+        call_s = []
         t0 = time.perf_counter()
         for j in range(args.steps):
+            t1 = time.perf_counter()
             eng.search_resident(qs[j % nq], 8)
+            call_s.append(time.perf_counter() - t1)
         dt = time.perf_counter() - t0
         if world > 1:
             import torch.distributed as dist
@@ -334,7 +350,8 @@ def main():
             dt = float(t.item())
         e2e = {"value": round(world * args.steps * bytes_per_step / dt / 1e9, 1), "unit": "GB/s",
                "h2d_bytes_per_step": d * 4, "d2h_bytes_per_step": result_d2h_bytes(8),
-               "p50_us": None, "ms_per_step": round(dt / args.steps * 1e3, 4)}
+               "p50_us": round(percentile(call_s, 50) * 1e6, 2), "p99_us": round(percentile(call_s, 99) * 1e6, 2),
+               "ms_per_step": round(dt / args.steps * 1e3, 4)}
 
     total_ms, k1_ms, step_ms = headline
     value = world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9

@@ -64,10 +64,10 @@ typedef enum rbf_status {
 /* Engine options for rbf_set_option (launch shape of the scoring kernel). */
 typedef enum rbf_option {
   RBF_OPT_CTAS_PER_SM = 1,   /* persistent CTAs per SM, 1..4 (default 1) */
-  RBF_OPT_STAGE_BYTES = 2,   /* target bytes per pipeline stage (default 32768) */
+  RBF_OPT_STAGE_BYTES = 2,   /* target bytes per pipeline stage (default 65536) */
   RBF_OPT_SMEM_BUDGET = 3,   /* shared-memory ring budget per CTA, bytes */
   RBF_OPT_TIMEOUT_NS = 4,    /* bound on every device-side wait (default 2e9) */
-  RBF_OPT_SCHEDULE = 5       /* 0 = static row ranges, 1 = dynamic tile claims */
+  RBF_OPT_SCHEDULE = 5       /* 0 = static row ranges, 1 = dynamic tile claims (default) */
 } rbf_option;
 
 /* ------------------------------------------------------------------ engine */

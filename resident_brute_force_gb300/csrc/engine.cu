@@ -65,10 +65,10 @@ struct rbf_engine {
 
   // Options.
   int ctas_per_sm = 1;
-  int stage_bytes = 32768;
+  int stage_bytes = 65536;
   int smem_budget = 0;  // 0: derived from the device limit
   uint64_t timeout_ns = 2000000000ull;
-  int dynamic = 0;
+  int dynamic = 1;
 
   // Last scoring launch (for merge_partial_topk_dev).
   int last_lists = 0;

@@ -6,18 +6,20 @@
 // (CUDA programming model series 9, section 3.1: one block over the GRID x K
 // stage-1 candidates).
 //
-// Each of the CTA's 32 warps folds a strided subset of the lists into a
-// register bitonic list (reversed max + bitonic merge per list), then the warp
-// lists are merged pairwise in shared memory, five levels, and warp 0 writes
-// the best K decoded. The keys already encode the ordering rule, so every
-// comparison is one unsigned 64-bit compare.
+// Each warp folds a strided subset of the lists into a register bitonic list
+// (reversed max + bitonic merge per list), loading the next list while it
+// merges the current one and reading only the first K entries of each list
+// (nothing past a list's K-th entry can reach the global top-K). The warp
+// lists are then merged pairwise in shared memory and warp 0 writes the best
+// K decoded. The keys already encode the ordering rule, so every comparison
+// is one unsigned 64-bit compare. The kernel is launched as a programmatic
+// dependent of the kernel that wrote the lists, so its launch overlaps that
+// kernel's tail; it waits for the lists before touching them.
 #include "rbf_device.cuh"
 #include "rbf_internal.h"
 
 namespace rbf {
 namespace {
-
-constexpr int kMergeWarps = 32;
 
 struct Params {
   const uint64_t* partials;
@@ -31,21 +33,47 @@ struct Params {
   int* result_err;
 };
 
-template <int KP>
-__global__ void __launch_bounds__(kMergeWarps * 32, 1) merge_partials_kernel(const Params p) {
+// List l's element KP-1-e for e = s*32 + lane, as the second operand of a
+// reversed-max fold; entries past the K-th read as the empty sentinel.
+template <int R>
+__device__ __forceinline__ void load_reversed(uint64_t (&dst)[R], const uint64_t* list, int k, int lane) {
+  constexpr int KP = 32 * R;
+#pragma unroll
+  for (int s = 0; s < R; ++s) {
+    const int e = KP - 1 - (s * 32 + lane);
+    dst[s] = (e < k) ? __ldcg(list + e) : 0ull;
+  }
+}
+
+template <int KP, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Params p) {
   constexpr int R = KP / 32;
   extern __shared__ __align__(16) uint64_t lists[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_wait();
   const uint64_t* base = p.partials + static_cast<size_t>(blockIdx.x) * p.lists * KP;
 
   uint64_t v[R];
   warp_list_clear<R>(v);
-  for (int l = warp; l < p.lists; l += kMergeWarps) warp_list_merge_from<R>(v, base + static_cast<size_t>(l) * KP, lane);
+  uint64_t nxt[R];
+  int l = warp;
+  if (l < p.lists) load_reversed<R>(nxt, base + static_cast<size_t>(l) * KP, p.k, lane);
+  while (l < p.lists) {
+    uint64_t cur[R];
+#pragma unroll
+    for (int s = 0; s < R; ++s) cur[s] = nxt[s];
+    const int ln = l + WARPS;
+    if (ln < p.lists) load_reversed<R>(nxt, base + static_cast<size_t>(ln) * KP, p.k, lane);
+#pragma unroll
+    for (int s = 0; s < R; ++s) v[s] = umax64(v[s], cur[s]);
+    warp_bitonic_merge_desc<R>(v, lane);
+    l = ln;
+  }
   warp_list_store<R>(v, lists + warp * KP, lane);
   __syncthreads();
 #pragma unroll
-  for (int step = 1; step < kMergeWarps; step <<= 1) {
+  for (int step = 1; step < WARPS; step <<= 1) {
     if ((warp % (2 * step)) == 0) {
       warp_list_merge_from<R>(v, lists + (warp + step) * KP, lane);
       warp_list_store<R>(v, lists + warp * KP, lane);
@@ -78,18 +106,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 1) merge_partials_kernel(con
   }
 }
 
-template <int KP>
+template <int KP, int WARPS>
 cudaError_t launch_t(const Params& p, int queries, cudaStream_t stream) {
-  auto fn = merge_partials_kernel<KP>;
-  const int smem = kMergeWarps * KP * 8;
+  auto fn = merge_partials_kernel<KP, WARPS>;
+  const int smem = WARPS * KP * 8;
   static int configured = 0;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  fn<<<queries, kMergeWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(queries));
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace
@@ -106,10 +143,10 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
   switch (list_width(a.k)) {
-    case 32: return launch_t<32>(p, a.queries, stream);
-    case 64: return launch_t<64>(p, a.queries, stream);
-    case 128: return launch_t<128>(p, a.queries, stream);
-    case 256: return launch_t<256>(p, a.queries, stream);
+    case 32: return launch_t<32, 32>(p, a.queries, stream);
+    case 64: return launch_t<64, 32>(p, a.queries, stream);
+    case 128: return launch_t<128, 32>(p, a.queries, stream);
+    case 256: return launch_t<256, 16>(p, a.queries, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -126,6 +126,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream is still
+// running; pdl_wait() blocks until that kernel has finished and its writes are
+// visible. pdl_launch_dependents() lets the next kernel be scheduled early.
+// Both are no-ops when the launch carries no such dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // L2 policy for data read exactly once per call: evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int RS = p.rows_per_stage;
+  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for us
 
   if (threadIdx.x == 0) {
     abort_flag = 0;

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   WarpBuffer& buf = bufs[warp];
+  pdl_launch_dependents();
 
   // Split into scalar head | 16-byte vectors | scalar tail.
   const uintptr_t addr = reinterpret_cast<uintptr_t>(data);
