@@ -8,6 +8,7 @@
 // per-query kernels are the fused score + partial select kernel and the merge
 // kernel (score_select.cu, merge.cu); the flat int32 path is topk_i32.cu +
 // merge.cu.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -49,6 +50,16 @@ struct rbf_engine {
   int d = 0;
   int pitch = 0;
   bool ready = false;
+
+  // bf16 copies for the batched path (RBF_FLAG_BF16_CORPUS).
+  void* corpus_bf16 = nullptr;   // max_n x max_pitch_bf16
+  void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
+  int max_pitch_bf16 = 0;
+  int pitch_bf16 = 0;
+  int query_rows = 0;            // max_batch rounded up to 256
+  alignas(64) CUtensorMap tmap_corpus;
+  alignas(64) CUtensorMap tmap_query;
+  bool tmaps_ready = false;
 
   // Workspaces (device).
   float* query = nullptr;        // max_batch * max_pitch floats
@@ -218,6 +229,8 @@ void release(rbf_engine* e) {
   if (!e) return;
   if (e->stream) cudaStreamSynchronize(e->stream);
   cudaFree(e->corpus);
+  cudaFree(e->corpus_bf16);
+  cudaFree(e->query_bf16);
   cudaFree(e->query);
   cudaFree(e->partials);
   cudaFree(e->errw);
@@ -285,12 +298,24 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   const size_t kpmax = static_cast<size_t>(list_width(max_k));
   const size_t max_lists = static_cast<size_t>(e->num_sms) * kMaxCtasPerSm;
   e->partials_cap = max_lists * kpmax;
+  if (flags & RBF_FLAG_BF16_CORPUS) {
+    flags |= RBF_FLAG_FP32_CORPUS;  // uploads are converted from the fp32 copy
+    e->flags = flags;
+    e->max_pitch_bf16 = static_cast<int>(align_up(static_cast<size_t>(max_d), kBf16PitchAlign));
+    e->query_rows = static_cast<int>(align_up(static_cast<size_t>(max_batch), kBatchQueriesPerLaunch));
+    const size_t batch_keys = static_cast<size_t>(max_batch) * e->num_sms * kBatchListWidth;
+    e->partials_cap = std::max(e->partials_cap, batch_keys);
+  }
   const size_t result_count = static_cast<size_t>(max_batch) * max_k;
   e->result_bytes = result_layout(result_count, 8).bytes;
 
   bool ok = true;
   if (flags & RBF_FLAG_FP32_CORPUS)
     ok = ok && cudaMalloc(&e->corpus, static_cast<size_t>(max_n) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  if (flags & RBF_FLAG_BF16_CORPUS) {
+    ok = ok && cudaMalloc(&e->corpus_bf16, static_cast<size_t>(max_n) * e->max_pitch_bf16 * 2) == cudaSuccess;
+    ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
+  }
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
@@ -382,6 +407,17 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
     RBF_COPY(e, cudaMemset2DAsync(e->corpus + d, static_cast<size_t>(pitch) * 4, 0,
                                   static_cast<size_t>(pitch - d) * 4, static_cast<size_t>(n), e->stream));
   }
+  if (e->corpus_bf16) {
+    const int pb = static_cast<int>(align_up(static_cast<size_t>(d), kBf16PitchAlign));
+    RBF_LAUNCH(e, launch_to_bf16(e->corpus, pitch, e->corpus_bf16, pb, n, n, d, e->num_sms, e->stream));
+    if (!make_bf16_tensor_map(&e->tmap_corpus, e->corpus_bf16, n, pb) ||
+        !make_bf16_tensor_map(&e->tmap_query, e->query_bf16, e->query_rows, pb)) {
+      e->tmaps_ready = false;
+      return RBF_ERR_CUDA;
+    }
+    e->pitch_bf16 = pb;
+    e->tmaps_ready = true;
+  }
   cudaError_t st = cudaStreamSynchronize(e->stream);
   if (st != cudaSuccess) return cuda_fail(e, st);
   e->n = n;
@@ -433,12 +469,44 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
   return RBF_OK;
 }
 
+// Batched search: convert the queries to bf16, run the tensor-core scoring +
+// epilogue select once per group of up to 256 queries, merge every query.
+static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, int k, int32_t* d_idx, float* d_score,
+                                int* result_err) {
+  if (!e->corpus_bf16) return RBF_ERR_UNSUPPORTED;
+  if (k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
+  if (!e->tmaps_ready) return RBF_ERR_NOT_READY;
+  const int64_t rows_total = static_cast<int64_t>(align_up(static_cast<size_t>(b), 128));
+  RBF_LAUNCH(e, launch_to_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d, e->num_sms,
+                               e->stream));
+  const int64_t tiles = (e->n + 127) / 128;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, e->num_sms)));
+  if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+  for (int q0 = 0; q0 < b; q0 += kBatchQueriesPerLaunch) {
+    GemmSelectLaunch a;
+    a.tmap_q = &e->tmap_query;
+    a.tmap_c = &e->tmap_corpus;
+    a.partials = e->partials;
+    a.err = e->errw;
+    a.n = e->n;
+    a.pitch_bf16 = e->pitch_bf16;
+    a.q_row0 = q0;
+    a.q_count = std::min(kBatchQueriesPerLaunch, b - q0);
+    a.q_out0 = q0;
+    a.k = k;
+    a.grid = grid;
+    a.timeout_ns = e->timeout_ns;
+    RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+  }
+  return enqueue_merge(e, k, grid, b, 0, d_idx, d_score, result_err);
+}
+
 rbf_status search_resident_batch_dev(rbf_engine* e, const float* d_queries, int32_t b, int32_t k, int32_t* d_idx,
                                      float* d_score) {
   if (!e || !d_queries || !d_idx || !d_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
-  return RBF_ERR_UNSUPPORTED;
+  return enqueue_batch(e, d_queries, b, k, d_idx, d_score, reinterpret_cast<int*>(e->result));
 }
 
 rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b, int32_t k, int32_t* out_idx,
@@ -446,7 +514,19 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (!e || !queries || !out_idx || !out_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
-  return RBF_ERR_UNSUPPORTED;
+  if (!e->corpus_bf16 || k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
+  const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
+  std::memcpy(e->h_query, queries, qbytes);
+  RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
+  const size_t count = static_cast<size_t>(b) * k;
+  const ResultLayout L = result_layout(count, 4);
+  if (rbf_status s = enqueue_batch(e, e->query, b, k, reinterpret_cast<int32_t*>(e->result + L.a_off),
+                                   reinterpret_cast<float*>(e->result + L.b_off), reinterpret_cast<int*>(e->result)))
+    return s;
+  if (rbf_status s = finish_host_call(e, L)) return s;
+  std::memcpy(out_idx, e->h_result + L.a_off, 4 * count);
+  std::memcpy(out_score, e->h_result + L.b_off, 4 * count);
+  return RBF_OK;
 }
 
 static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* val,

@@ -1,0 +1,527 @@
+// gemm_select.cu -- batched queries: bf16 tensor-core scoring with the top-K
+// selection fused into the epilogue.
+//
+// For a batch of queries the scoring S = Q * C^T is a dense contraction, so it
+// runs on the 5th-generation tensor cores (tcgen05): bf16 inputs, fp32
+// accumulators in tensor memory (TMEM). The selection is the same problem as
+// the single-query path (GPU-Resident Top-K for Agentic RAG, section 4 steps
+// 3-4: per-block partial top-K, then a merge): every CTA leaves one
+// best-first list per query, and the merge kernel finishes each query.
+//
+// One CTA per SM, 10 warps:
+//   warp 0     TMA producer: per 64-wide K chunk, the query tile(s) (up to
+//              256 queries = two 128-row M tiles) and 128 corpus rows, 128-byte
+//              swizzled, into a 4-stage shared-memory ring;
+//   warp 1     TMEM owner and MMA issuer: one thread issues
+//              tcgen05.mma.cta_group::1.kind::f16 (M = 128 queries, N = 128
+//              corpus rows, K = 16) into one of two accumulator buffers, so the
+//              epilogue drains tile t while tile t + 1 accumulates;
+//   warps 2-9  epilogue: thread = one query (its TMEM lane); it reads its 128
+//              scores 32 at a time (tcgen05.ld 32x32b.x32), keeps the keys that
+//              beat its K-th best in a 16-entry shared-memory buffer, and merges
+//              full buffers into a register bitonic list of KP <= 32 keys.
+// The scores never reach memory: each CTA writes 32 keys per query.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "rbf_device.cuh"
+#include "rbf_internal.h"
+
+namespace rbf {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileRows = 128;      // corpus rows per tile (MMA N)
+constexpr int kKChunk = 64;         // bf16 elements per 128-byte swizzle row
+constexpr int kSubTileBytes = 128 * kKChunk * 2;  // 16 KB: 128 rows x 128 B
+constexpr int kStageBytes = 3 * kSubTileBytes;    // A0 | A1 | B
+constexpr int kCandCap = 16;        // buffered candidates per query
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kTmemCols = 512;      // 2 buffers x 2 M tiles x 128 columns
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(smem) * B(smem)^T, both K-major bf16, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two-dimensional tiled TMA load (x = element offset along the row, y = row).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 128 bytes, groups of 8 rows 1024 bytes
+// apart (stride byte offset), leading byte offset unused (1), descriptor
+// version 1, layout SWIZZLE_128B (2). The tile base is 1024-byte aligned.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(const void* tile) {
+  const uint32_t a = smem_addr(tile);
+  uint64_t d = static_cast<uint64_t>((a >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
+// bf16 (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at
+// bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ------------------------------------------------- per-thread key lists
+
+// Descending bitonic sort of 8 keys in registers.
+__device__ __forceinline__ void sort8_desc(uint64_t (&c)[8]) {
+#pragma unroll
+  for (int k = 2; k <= 8; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t a = c[i], b = c[l];
+          const bool desc = (i & k) == 0;
+          c[i] = desc ? umax64(a, b) : umin64(a, b);
+          c[l] = desc ? umin64(a, b) : umax64(a, b);
+        }
+      }
+    }
+  }
+}
+
+// Fold 8 sorted candidates onto the last 8 slots of a descending list of KP
+// keys (reversed max) and restore the order with a bitonic merge.
+template <int KP>
+__device__ __forceinline__ void list_merge8(uint64_t (&L)[KP], const uint64_t (&c)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) L[KP - 8 + i] = umax64(L[KP - 8 + i], c[7 - i]);
+#pragma unroll
+  for (int j = KP / 2; j > 0; j >>= 1) {
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+      if ((i & j) == 0) {
+        const uint64_t a = L[i], b = L[i + j];
+        L[i] = umax64(a, b);
+        L[i + j] = umin64(a, b);
+      }
+    }
+  }
+}
+
+template <int KP>
+__device__ __forceinline__ uint64_t list_get(const uint64_t (&L)[KP], int e) {
+  uint64_t x = 0;
+#pragma unroll
+  for (int i = 0; i < KP; ++i)
+    if (i == e) x = L[i];
+  return x;
+}
+
+// Offer columns J0..J0+7 of a 32-column score chunk: a key that beats theta
+// goes into this thread's column of the shared candidate buffer. Rows arrive
+// in increasing order, so a score equal to theta's comes from a later row and
+// loses the tie: the strict float compare is an exact pre-test.
+template <int J0>
+__device__ __forceinline__ void offer8(const float (&sc)[32], int64_t row_base, int64_t n, uint64_t theta,
+                                       float theta_f, bool filling, uint64_t* cand, int slot, int& cnt) {
+#pragma unroll
+  for (int j = J0; j < J0 + 8; ++j) {
+    if (filling || sc[j] > theta_f) {
+      const int64_t row = row_base + j;
+      const uint64_t key = row < n ? make_key(sc[j], static_cast<uint32_t>(row)) : 0ull;
+      if (key > theta) {
+        cand[cnt * 256 + slot] = key;
+        ++cnt;
+      }
+    }
+  }
+}
+
+struct Params {
+  uint64_t* partials;  // [queries in batch][grid][32] keys
+  int* err;
+  int64_t n;           // corpus rows
+  int num_tiles;       // ceil(n / 128)
+  int kchunks;         // padded D / 64
+  int num_mt;          // 1 or 2 M tiles of 128 queries in this launch
+  int q_row0;          // first query row of this launch in the bf16 query buffer
+  int q_count;         // queries in this launch
+  int q_out0;          // first query of this launch in the partials layout
+  int k;
+  uint64_t timeout_ns;
+};
+
+template <int KP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_select_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
+                            const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);  // [kCandCap][256]
+  uint64_t* full = cand + kCandCap * 256;
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4 * p.num_mt);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // --------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_c = l2_policy_evict_first();
+      const uint64_t pol_q = l2_policy_evict_last();
+      const uint32_t bytes = static_cast<uint32_t>((p.num_mt + 1) * kSubTileBytes);
+      int64_t it = 0;
+      bool aborted = false;
+      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
+        for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
+          const int s = static_cast<int>(it % kStages);
+          const uint32_t u = static_cast<uint32_t>(it / kStages);
+          if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1u, p.timeout_ns)) {
+            atomicOr(p.err, kErrProducerTimeout);
+            aborted = true;
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+            aborted = true;
+            break;
+          }
+          uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d(st, &tmap_q, kc * kKChunk, p.q_row0, &full[s], pol_q);
+          if (p.num_mt > 1) tma_load_2d(st + kSubTileBytes, &tmap_q, kc * kKChunk, p.q_row0 + 128, &full[s], pol_q);
+          tma_load_2d(st + 2 * kSubTileBytes, &tmap_c, kc * kKChunk, t * kTileRows, &full[s], pol_c);
+        }
+      }
+      if (aborted) {
+        abort_flag = 1;
+        // Let every issued load land before the CTA can exit.
+        for (int64_t i = (it > kStages ? it - kStages : 0); i < it; ++i) {
+          const int s = static_cast<int>(i % kStages);
+          if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kStages) & 1u, p.timeout_ns))
+            atomicOr(p.err, kErrDrainTimeout);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(128, kTileRows);
+      int64_t it = 0;
+      int tile_i = 0;
+      bool aborted = false;
+      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x, ++tile_i) {
+        const int b = tile_i & 1;
+        const uint32_t ub = static_cast<uint32_t>(tile_i >> 1);
+        if (ub > 0 && !mbar_wait(&acc_empty[b], (ub - 1) & 1u, p.timeout_ns)) {
+          atomicOr(p.err, kErrConsumerTimeout);
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
+          const int s = static_cast<int>(it % kStages);
+          if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, p.timeout_ns)) {
+            atomicOr(p.err, kErrConsumerTimeout);
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
+          const uint64_t bdesc = sw128_kmajor_desc(st + 2 * kSubTileBytes);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            if (m < p.num_mt) {
+              const uint64_t adesc = sw128_kmajor_desc(st + m * kSubTileBytes);
+              const uint32_t d = tmem_base + static_cast<uint32_t>(b * 256 + m * 128);
+#pragma unroll
+              for (int k = 0; k < kKChunk / 16; ++k) {
+                // Advance both descriptors 32 bytes (16 bf16) along K.
+                umma_bf16(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                          (kc | k) != 0);
+              }
+            }
+          }
+          umma_commit(&empty[s]);  // the stage is free once these MMAs finish
+        }
+        if (aborted) break;
+        umma_commit(&acc_full[b]);  // the accumulator is complete
+      }
+      if (aborted) abort_flag = 1;
+      // Every MMA issued must be finished before TMEM is released.
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0, p.timeout_ns)) atomicOr(p.err, kErrDrainTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int e = warp - 2;
+    const int m = e >> 2;             // M tile
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int qlocal = m * 128 + quad * 32 + lane;
+    const int slot = qlocal;          // candidate buffer column
+    uint64_t L[KP];
+#pragma unroll
+    for (int i = 0; i < KP; ++i) L[i] = 0;
+    uint64_t theta = 0;
+    float theta_f = 0.0f;
+    bool filling = true;
+    int cnt = 0;
+
+    // Merge every buffered candidate into the list, 8 at a time, for as many
+    // batches as the fullest lane of the warp needs.
+    auto merge_buffer = [&]() {
+      const int batches = static_cast<int>((__reduce_max_sync(kFullMask, static_cast<unsigned>(cnt)) + 7u) >> 3);
+#pragma unroll 1
+      for (int b8 = 0; b8 < batches * 8; b8 += 8) {
+        uint64_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = (b8 + i < cnt) ? cand[(b8 + i) * 256 + slot] : 0ull;
+        sort8_desc(c);
+        list_merge8<KP>(L, c);
+      }
+      cnt = 0;
+      theta = list_get<KP>(L, p.k - 1);
+      filling = theta == 0;
+      theta_f = filling ? 0.0f : key_score(theta);
+    };
+
+    if (m < p.num_mt) {
+      int tile_i = 0;
+      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
+        const int b = tile_i & 1;
+        if (!__all_sync(kFullMask, mbar_wait(&acc_full[b], static_cast<uint32_t>(tile_i >> 1) & 1u, p.timeout_ns))) {
+          if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
+          abort_flag = 1;
+          break;
+        }
+        if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) break;
+        tc_fence_after();
+        const int64_t row0 = static_cast<int64_t>(t) * kTileRows;
+#pragma unroll 1
+        for (int c = 0; c < kTileRows / 32; ++c) {
+          float sc[32];
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                 static_cast<uint32_t>(b * 256 + m * 128 + c * 32);
+          tmem_ld32(taddr, sc);
+          const int64_t rb = row0 + c * 32;
+          // Four groups of 8 columns with one merge point: the buffer (16
+          // slots) holds at most 7 + 8 keys, and the merge code exists once.
+#pragma unroll 1
+          for (int g = 0; g < 4; ++g) {
+            switch (g) {
+              case 0: offer8<0>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
+              case 1: offer8<8>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
+              case 2: offer8<16>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
+              default: offer8<24>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
+            }
+            if (__any_sync(kFullMask, cnt >= 8)) merge_buffer();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+      }
+      if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
+      if (qlocal < p.q_count) {
+        uint64_t* dst = p.partials + (static_cast<size_t>(p.q_out0 + qlocal) * gridDim.x + blockIdx.x) * 32;
+#pragma unroll
+        for (int i = 0; i < KP; ++i) dst[i] = L[i];
+#pragma unroll
+        for (int i = KP; i < 32; ++i) dst[i] = 0ull;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// --------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <int KP>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
+  auto fn = gemm_select_bf16_kernel<KP>;
+  const int smem = gemm_select_smem_bytes();
+  static int configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  fn<<<grid, kThreads, smem, st>>>(tq, tc, p);
+  return cudaGetLastError();
+}
+
+// fp32 [rows][src_pitch] -> bf16 [rows][dst_pitch], zero past `cols` and for
+// rows in [rows, rows_total).
+__global__ void to_bf16_kernel(const float* __restrict__ src, int64_t src_pitch, __nv_bfloat16* __restrict__ dst,
+                               int64_t dst_pitch, int64_t rows, int64_t rows_total, int cols) {
+  const int64_t total = rows_total * dst_pitch;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / dst_pitch;
+    const int64_t c = i - r * dst_pitch;
+    const float v = (r < rows && c < cols) ? src[r * src_pitch + c] : 0.0f;
+    dst[i] = __float2bfloat16_rn(v);
+  }
+}
+
+}  // namespace
+
+int gemm_select_smem_bytes() {
+  return 1024 + kStages * kStageBytes + kCandCap * 256 * 8 + (2 * kStages + 5) * 8 + 16;
+}
+
+bool make_bf16_tensor_map(void* map_out, const void* base, int64_t rows, int pitch_elems) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pitch_elems), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKChunk), 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,
+                           int64_t rows_total, int cols, int num_sms, cudaStream_t st) {
+  const int64_t total = rows_total * dst_pitch;
+  int64_t blocks = (total + 255) / 256;
+  blocks = blocks < int64_t(num_sms) * 8 ? blocks : int64_t(num_sms) * 8;
+  if (blocks < 1) blocks = 1;
+  to_bf16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, static_cast<__nv_bfloat16*>(dst),
+                                                          dst_pitch, rows, rows_total, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
+  Params p;
+  p.partials = a.partials;
+  p.err = a.err;
+  p.n = a.n;
+  p.num_tiles = static_cast<int>((a.n + kTileRows - 1) / kTileRows);
+  p.kchunks = a.pitch_bf16 / kKChunk;
+  p.num_mt = a.q_count > 128 ? 2 : 1;
+  p.q_row0 = a.q_row0;
+  p.q_count = a.q_count;
+  p.q_out0 = a.q_out0;
+  p.k = a.k;
+  p.timeout_ns = a.timeout_ns;
+  const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
+  const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
+  if (a.k <= 8) return launch_t<8>(tq, tc, p, a.grid, stream);
+  if (a.k <= 16) return launch_t<16>(tq, tc, p, a.grid, stream);
+  if (a.k <= 32) return launch_t<32>(tq, tc, p, a.grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace rbf

@@ -66,4 +66,33 @@ cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(int* err, uint64_t timeout_ns, cudaStream_t stream);
 
+// Batched queries (tensor cores). K <= 32; each launch covers up to 256
+// queries; every CTA writes 32 keys per query.
+constexpr int kBatchMaxK = 32;
+constexpr int kBatchQueriesPerLaunch = 256;
+constexpr int kBatchListWidth = 32;
+constexpr int kBf16PitchAlign = 64;  // bf16 elements: one 128-byte swizzle row
+
+struct GemmSelectLaunch {
+  const void* tmap_q;        // host CUtensorMap over the bf16 query buffer
+  const void* tmap_c;        // host CUtensorMap over the bf16 corpus
+  uint64_t* partials;        // [queries][grid][32] keys
+  int* err;
+  int64_t n;                 // corpus rows
+  int pitch_bf16;            // padded D, a multiple of 64
+  int q_row0;                // first query row of this launch in the query buffer
+  int q_count;               // queries in this launch, 1..256
+  int q_out0;                // first query of this launch in the partials layout
+  int k;
+  int grid;
+  uint64_t timeout_ns;
+};
+int gemm_select_smem_bytes();
+// Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
+bool make_bf16_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);
+cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream);
+// fp32 [rows][src_pitch] -> bf16 [rows_total][dst_pitch] (RN-even), zero padded.
+cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,
+                           int64_t rows_total, int cols, int num_sms, cudaStream_t stream);
+
 }  // namespace rbf

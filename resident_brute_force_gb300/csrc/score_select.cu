@@ -170,8 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
     for (int64_t i = 0;; ++i) {
       const int s = static_cast<int>(i % p.stages);
       const uint32_t u = static_cast<uint32_t>(i / p.stages);
-      if (!mbar_wait(&full[s], u & 1u, p.timeout_ns)) {
-        atomicOr(p.err, kErrConsumerTimeout);
+      // Every lane polls; the verdict is made warp-uniform so a timeout can
+      // never split the warp ahead of the full-mask shuffles below.
+      if (!__all_sync(kFullMask, mbar_wait(&full[s], u & 1u, p.timeout_ns))) {
+        if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
         abort_flag = 1;
         break;
       }

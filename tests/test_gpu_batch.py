@@ -1,0 +1,133 @@
+"""Batched search (tcgen05 bf16 scoring + fused epilogue select) through the C
+ABI against the oracle.
+
+Two references: the oracle on the original fp32 data (the true answer; rule:
+2e-2 absolute on unit-norm data) and the oracle on the bf16-rounded corpus and
+queries (what the tensor cores multiply; products are exact in fp32, so only
+the fp32 accumulation differs: 1e-4 absolute). Dyadic inputs are exact in bf16
+and their sums exact in fp32, so there the result must match bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests.parity import BF16_ABS, check_exact, check_float_topk, check_sorted_distinct
+
+pytestmark = pytest.mark.gpu
+
+BF16_ACC_ABS = 1e-4
+
+
+@pytest.fixture(scope="module")
+def rbf():
+    import resident_brute_force_gb300 as rbf
+    rbf.load_library()
+    return rbf
+
+
+def engine(rbf, n, d, b, k=32):
+    return rbf.Engine(n, d, k, max_batch=b, flags=rbf.RBF_FLAG_BF16_CORPUS)
+
+
+@pytest.mark.parametrize("n,d,b,k", [
+    (1000, 64, 5, 8), (300, 128, 1, 1), (4099, 768, 130, 32), (2000, 100, 256, 16), (777, 64, 300, 32),
+])
+def test_dyadic_bit_exact(rbf, n, d, b, k):
+    c = workloads.dyadic_grid(n, d, seed=n + d)
+    qs = workloads.dyadic_grid(b, d, seed=n + d + 1)
+    with engine(rbf, n, d, b, 32) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, k)
+        for j in range(b):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], k))
+
+
+@pytest.mark.parametrize("d", [768, 384, 1024])
+def test_unit_gaussian_both_references(rbf, d):
+    n, b, k = 20_011, 256, 32
+    c = workloads.unit_corpus(n, d, seed=1)
+    qs = workloads.unit_queries(b, d, seed=2)
+    c16 = oracle.round_bf16(c)
+    q16 = oracle.round_bf16(qs)
+    with engine(rbf, n, d, b) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, k)
+        for j in range(0, b, 17):
+            sig16 = oracle.scores(c16, q16[j])
+            check_float_topk(idx[j], sc[j], sig16, k, tol_abs=BF16_ACC_ABS)
+            sig = oracle.scores(c, qs[j])
+            check_float_topk(idx[j], sc[j], sig, k, tol_abs=BF16_ABS)
+
+
+def test_duplicates_and_ties(rbf):
+    rng = np.random.default_rng(5)
+    base = workloads.dyadic_grid(40, 128, seed=6)
+    c = base[rng.integers(0, 40, size=5000)]
+    qs = workloads.dyadic_grid(64, 128, seed=7)
+    with engine(rbf, 5000, 128, 64) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, 32)
+        for j in range(64):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], 32))
+
+
+def test_dev_matches_host_and_repeats(rbf):
+    import torch
+    n, d, b = 30_000, 768, 200
+    c = workloads.unit_corpus(n, d, seed=11)
+    qs = workloads.unit_queries(b, d, seed=12)
+    with engine(rbf, n, d, b) as e:
+        e.upload_corpus_rowmajor(c)
+        h_idx, h_sc = e.search_resident_batch(qs, 32)
+        dq = torch.from_numpy(qs).cuda()
+        d_idx = torch.empty((b, 32), dtype=torch.int32, device="cuda")
+        d_sc = torch.empty((b, 32), dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            e.search_resident_batch_dev(dq, 32, d_idx, d_sc)
+            torch.cuda.synchronize()
+            assert np.array_equal(d_idx.cpu().numpy(), h_idx)
+            assert np.array_equal(d_sc.cpu().numpy(), h_sc)
+        assert e.check_device_error() == rbf.RBF_OK
+
+
+def test_unsupported_and_invalid(rbf):
+    c = workloads.dyadic_grid(500, 64, seed=21)
+    qs = workloads.dyadic_grid(4, 64, seed=22)
+    with rbf.Engine(500, 64, 64, max_batch=4) as e:      # no bf16 copy
+        e.upload_corpus_rowmajor(c)
+        with pytest.raises(rbf.RbfError) as ei:
+            e.search_resident_batch(qs, 8)
+        assert ei.value.status == rbf.RBF_ERR_UNSUPPORTED
+    with engine(rbf, 500, 64, 4, k=64) as e:
+        e.upload_corpus_rowmajor(c)
+        with pytest.raises(rbf.RbfError) as ei:
+            e.search_resident_batch(qs, 33)             # the fused select keeps K <= 32
+        assert ei.value.status == rbf.RBF_ERR_UNSUPPORTED
+        with pytest.raises(rbf.RbfError) as ei:
+            e.search_resident_batch(np.concatenate([qs, qs]), 8)
+        assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
+        idx, sc = e.search_resident_batch(qs, 8)
+        for j in range(4):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], 8))
+
+
+def test_full_size_planted(rbf):
+    """B = 256 queries x N = 1,000,000 x D = 768, K = 32, with 10 planted
+    near-duplicates per query: planted rows lead for every query, and a sample
+    of queries matches both oracle references."""
+    n, d, b, k = 1_000_000, 768, 256, 32
+    c = workloads.unit_corpus(n, d, seed=1)
+    qs = workloads.unit_queries(b, d, seed=2)
+    planted = workloads.plant_near_duplicates(c, qs, per_query=10, noise=0.05, seed=3)
+    with engine(rbf, n, d, b) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, k)
+        for j in range(b):
+            assert set(idx[j][:10].tolist()) == set(planted[j].tolist()), j
+            check_sorted_distinct(idx[j].astype(np.int64), sc[j].astype(np.float64), n)
+        c16 = oracle.round_bf16(c)
+        for j in (0, 97, 255):
+            q16 = oracle.round_bf16(qs[j])
+            check_float_topk(idx[j], sc[j], oracle.scores(c16, q16), k, tol_abs=BF16_ACC_ABS)
+            check_float_topk(idx[j], sc[j], oracle.scores(c, qs[j]), k, tol_abs=BF16_ABS)
