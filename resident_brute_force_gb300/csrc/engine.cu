@@ -27,6 +27,7 @@ constexpr int kMaxBatch = 4096;
 constexpr int kResultHeader = 16;  // error word + padding, ahead of the results
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kI32CtasPerSm = 2;
+constexpr int64_t kSampleRows = 16384;  // rows of the batched path's threshold pre-pass
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -54,6 +55,7 @@ struct rbf_engine {
   // bf16 copies for the batched path (RBF_FLAG_BF16_CORPUS).
   void* corpus_bf16 = nullptr;   // max_n x max_pitch_bf16
   void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
+  uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
@@ -231,6 +233,7 @@ void release(rbf_engine* e) {
   cudaFree(e->corpus);
   cudaFree(e->corpus_bf16);
   cudaFree(e->query_bf16);
+  cudaFree(e->theta0);
   cudaFree(e->query);
   cudaFree(e->partials);
   cudaFree(e->errw);
@@ -315,6 +318,7 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   if (flags & RBF_FLAG_BF16_CORPUS) {
     ok = ok && cudaMalloc(&e->corpus_bf16, static_cast<size_t>(max_n) * e->max_pitch_bf16 * 2) == cudaSuccess;
     ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
+    ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
   }
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
@@ -479,25 +483,56 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   const int64_t rows_total = static_cast<int64_t>(align_up(static_cast<size_t>(b), 128));
   RBF_LAUNCH(e, launch_to_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d, e->num_sms,
                                e->stream));
-  const int64_t tiles = (e->n + 127) / 128;
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, e->num_sms)));
-  if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;
-  for (int q0 = 0; q0 < b; q0 += kBatchQueriesPerLaunch) {
-    GemmSelectLaunch a;
-    a.tmap_q = &e->tmap_query;
-    a.tmap_c = &e->tmap_corpus;
-    a.partials = e->partials;
-    a.err = e->errw;
-    a.n = e->n;
-    a.pitch_bf16 = e->pitch_bf16;
-    a.q_row0 = q0;
-    a.q_count = std::min(kBatchQueriesPerLaunch, b - q0);
-    a.q_out0 = q0;
-    a.k = k;
-    a.grid = grid;
-    a.timeout_ns = e->timeout_ns;
-    RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+  // The scoring + select kernel over rows [0, rows): one launch per group of
+  // up to 256 queries; returns the number of per-CTA lists per query.
+  auto score_groups = [&](int64_t rows, const uint64_t* theta0, int* lists) -> rbf_status {
+    const int64_t tiles = (rows + 127) / 128;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, e->num_sms)));
+    if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+    for (int q0 = 0; q0 < b; q0 += kBatchQueriesPerLaunch) {
+      GemmSelectLaunch a;
+      a.tmap_q = &e->tmap_query;
+      a.tmap_c = &e->tmap_corpus;
+      a.partials = e->partials;
+      a.err = e->errw;
+      a.n = rows;
+      a.pitch_bf16 = e->pitch_bf16;
+      a.q_row0 = q0;
+      a.q_count = std::min(kBatchQueriesPerLaunch, b - q0);
+      a.q_out0 = q0;
+      a.k = k;
+      a.grid = grid;
+      a.timeout_ns = e->timeout_ns;
+      a.theta0 = theta0;
+      RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+    }
+    *lists = grid;
+    return RBF_OK;
+  };
+  // Pre-pass: the exact K-th best key of every query over the first
+  // kSampleRows rows. It is a lower bound on the final K-th key (those rows
+  // are part of the corpus), so the main pass drops every key below it.
+  const uint64_t* theta0 = nullptr;
+  if (e->n >= 4 * kSampleRows) {
+    int lists = 0;
+    if (rbf_status st = score_groups(kSampleRows, nullptr, &lists)) return st;
+    MergeLaunch m;
+    m.partials = e->partials;
+    m.lists = lists;
+    m.queries = b;
+    m.k = k;
+    m.int_keys = 0;
+    m.out_a = d_idx;  // overwritten by the final merge
+    m.out_b = d_score;
+    m.err_call = nullptr;
+    m.err_sticky = nullptr;
+    m.result_err = nullptr;
+    m.kth_out = e->theta0;
+    RBF_LAUNCH(e, launch_merge(m, e->stream));
+    theta0 = e->theta0;
   }
+  int grid = 0;
+  if (rbf_status st = score_groups(e->n, theta0, &grid)) return st;
   return enqueue_merge(e, k, grid, b, 0, d_idx, d_score, result_err);
 }
 

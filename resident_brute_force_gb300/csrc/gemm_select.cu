@@ -179,23 +179,20 @@ __device__ __forceinline__ uint64_t list_get(const uint64_t (&L)[KP], int e) {
   return x;
 }
 
-// Offer columns J0..J0+7 of a 32-column score chunk: a key that beats theta
-// goes into this thread's column of the shared candidate buffer. Rows arrive
-// in increasing order, so a score equal to theta's comes from a later row and
-// loses the tie: the strict float compare is an exact pre-test.
-template <int J0>
-__device__ __forceinline__ void offer8(const float (&sc)[32], int64_t row_base, int64_t n, uint64_t theta,
-                                       float theta_f, bool filling, uint64_t* cand, int slot, int& cnt) {
-#pragma unroll
-  for (int j = J0; j < J0 + 8; ++j) {
-    if (filling || sc[j] > theta_f) {
-      const int64_t row = row_base + j;
-      const uint64_t key = row < n ? make_key(sc[j], static_cast<uint32_t>(row)) : 0ull;
-      if (key > theta) {
-        cand[cnt * 256 + slot] = key;
-        ++cnt;
-      }
-    }
+// sc[j] for a warp-uniform j: a switch keeps the scores in registers (a
+// dynamically indexed register array would live in local memory).
+__device__ __forceinline__ float pick(const float (&sc)[32], int j) {
+  switch (j) {
+#define RBF_PICK(i) \
+  case i:           \
+    return sc[i];
+    RBF_PICK(0) RBF_PICK(1) RBF_PICK(2) RBF_PICK(3) RBF_PICK(4) RBF_PICK(5) RBF_PICK(6) RBF_PICK(7)
+    RBF_PICK(8) RBF_PICK(9) RBF_PICK(10) RBF_PICK(11) RBF_PICK(12) RBF_PICK(13) RBF_PICK(14) RBF_PICK(15)
+    RBF_PICK(16) RBF_PICK(17) RBF_PICK(18) RBF_PICK(19) RBF_PICK(20) RBF_PICK(21) RBF_PICK(22) RBF_PICK(23)
+    RBF_PICK(24) RBF_PICK(25) RBF_PICK(26) RBF_PICK(27) RBF_PICK(28) RBF_PICK(29) RBF_PICK(30)
+#undef RBF_PICK
+    default:
+      return sc[31];
   }
 }
 
@@ -211,6 +208,7 @@ struct Params {
   int q_out0;          // first query of this launch in the partials layout
   int k;
   uint64_t timeout_ns;
+  const uint64_t* theta0;  // optional per-query lower bound on the K-th key
 };
 
 template <int KP>
@@ -354,9 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t L[KP];
 #pragma unroll
     for (int i = 0; i < KP; ++i) L[i] = 0;
-    uint64_t theta = 0;
-    float theta_f = 0.0f;
-    bool filling = true;
+    // theta: every key <= theta is dropped. Without a bound it starts at the
+    // empty key (everything passes until K keys are held). With a bound b on
+    // the final K-th key (the K-th best of a row sample), keys >= b can still
+    // make the top K, so theta starts at b - 1.
+    uint64_t floor_key = 0;
+    if (p.theta0 && qlocal < p.q_count) {
+      const uint64_t b0 = p.theta0[p.q_out0 + qlocal];
+      floor_key = b0 > 0 ? b0 - 1 : 0;
+    }
+    uint64_t theta = floor_key;
+    float theta_f = floor_key ? key_score(floor_key + 1) : 0.0f;
+    bool filling = floor_key == 0;
     int cnt = 0;
 
     // Merge every buffered candidate into the list, 8 at a time, for as many
@@ -372,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         list_merge8<KP>(L, c);
       }
       cnt = 0;
-      theta = list_get<KP>(L, p.k - 1);
+      theta = umax64(list_get<KP>(L, p.k - 1), floor_key);
       filling = theta == 0;
-      theta_f = filling ? 0.0f : key_score(theta);
+      theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
     };
 
     if (m < p.num_mt) {
@@ -396,17 +403,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  static_cast<uint32_t>(b * 256 + m * 128 + c * 32);
           tmem_ld32(taddr, sc);
           const int64_t rb = row0 + c * 32;
-          // Four groups of 8 columns with one merge point: the buffer (16
-          // slots) holds at most 7 + 8 keys, and the merge code exists once.
-#pragma unroll 1
-          for (int g = 0; g < 4; ++g) {
-            switch (g) {
-              case 0: offer8<0>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
-              case 1: offer8<8>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
-              case 2: offer8<16>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
-              default: offer8<24>(sc, rb, p.n, theta, theta_f, filling, cand, slot, cnt); break;
+          // One bit per column whose score may beat theta (a superset test:
+          // ties are settled below by the key compare), built without
+          // branches; rows past the corpus end are masked off.
+          uint32_t m = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
+          if (filling) m = 0xFFFFFFFFu;
+          if (p.n - rb < 32) m &= (p.n - rb > 0) ? ((1u << (p.n - rb)) - 1u) : 0u;
+          // Walk the columns any lane flagged, in order, warp-uniformly.
+          uint32_t u = __reduce_or_sync(kFullMask, m);
+          while (u) {
+            const int j = __ffs(u) - 1;
+            u &= u - 1;
+            if (m & (1u << j)) {
+              const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j));
+              if (key > theta) {
+                cand[cnt * 256 + slot] = key;
+                ++cnt;
+              }
             }
-            if (__any_sync(kFullMask, cnt >= 8)) merge_buffer();
+            if (__any_sync(kFullMask, cnt == kCandCap)) merge_buffer();
           }
         }
         tc_fence_before();
@@ -516,6 +533,7 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.q_out0 = a.q_out0;
   p.k = a.k;
   p.timeout_ns = a.timeout_ns;
+  p.theta0 = a.theta0;
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
   if (a.k <= 8) return launch_t<8>(tq, tc, p, a.grid, stream);

@@ -31,6 +31,7 @@ struct Params {
   int* err_call;
   int* err_sticky;
   int* result_err;
+  uint64_t* kth_out;  // optional: the K-th key of each query
 };
 
 // List l's element KP-1-e for e = s*32 + lane, as the second operand of a
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
 #pragma unroll
     for (int s = 0; s < R; ++s) {
       const int e = s * 32 + lane;
+      if (p.kth_out && e == p.k - 1) p.kth_out[blockIdx.x] = v[s];
       if (e < p.k) {
         const size_t o = static_cast<size_t>(blockIdx.x) * p.k + e;
         if (p.int_keys) {
@@ -142,6 +144,7 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.err_call = a.err_call;
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
+  p.kth_out = a.kth_out;
   switch (list_width(a.k)) {
     case 32: return launch_t<32, 32>(p, a.queries, stream);
     case 64: return launch_t<64, 32>(p, a.queries, stream);

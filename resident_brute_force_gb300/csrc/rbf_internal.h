@@ -52,6 +52,7 @@ struct MergeLaunch {
   int* err_call;             // per-call error word, moved out and cleared
   int* err_sticky;           // sticky error word (ORed)
   int* result_err;           // where the per-call error lands (may be null)
+  uint64_t* kth_out = nullptr;  // optional: each query's K-th key
 };
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
 
@@ -86,6 +87,7 @@ struct GemmSelectLaunch {
   int k;
   int grid;
   uint64_t timeout_ns;
+  const uint64_t* theta0;    // optional per-query lower bound on the K-th key (keys >= it are kept)
 };
 int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.

@@ -131,3 +131,51 @@ def test_full_size_planted(rbf):
             q16 = oracle.round_bf16(qs[j])
             check_float_topk(idx[j], sc[j], oracle.scores(c16, q16), k, tol_abs=BF16_ACC_ABS)
             check_float_topk(idx[j], sc[j], oracle.scores(c, qs[j]), k, tol_abs=BF16_ABS)
+
+
+# N >= 65,536 rows: the batched path first finds each query's K-th best key over
+# the first 16,384 rows and drops every key below it in the main pass.
+
+@pytest.mark.parametrize("k", [1, 8, 32])
+def test_sample_bound_dyadic_exact(rbf, k):
+    n, d, b = 70_001, 64, 40
+    c = workloads.dyadic_grid(n, d, seed=31)
+    qs = workloads.dyadic_grid(b, d, seed=32)
+    with engine(rbf, n, d, b) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, k)
+        for j in range(b):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], k))
+
+
+def test_sample_bound_best_rows_outside_sample(rbf):
+    """Row i is (alpha_i, 0, ..., 0) with alpha_i = floor(255 i / n), exact in
+    bf16: the sample (the first rows) holds only small alphas, so for a query
+    along +e0 the bound is weak and almost every row passes it, and the answer
+    (the first 32 rows with alpha = 254) lies outside the sample."""
+    n, d = 80_000, 64
+    c = np.zeros((n, d), dtype=np.float32)
+    c[:, 0] = np.floor(np.arange(n) * 255.0 / n)
+    e0 = np.zeros(d, dtype=np.float32)
+    e0[0] = 1.0
+    qs = np.stack([e0, -e0, workloads.dyadic_grid(1, d, seed=42)[0]])
+    with engine(rbf, n, d, 3) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, 32)
+        for j in range(3):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], 32))
+        first = int(np.argmax(c[:, 0] == 254.0))
+        assert idx[0].tolist() == list(range(first, first + 32))
+
+
+def test_sample_bound_all_equal_rows(rbf):
+    """Every row ties: the K-th key of the sample is row K-1 itself, and the
+    answer is rows 0..K-1, all inside the sample."""
+    n, d = 70_000, 64
+    c = np.full((n, d), 0.25, dtype=np.float32)
+    qs = np.ones((2, d), dtype=np.float32)
+    with engine(rbf, n, d, 2) as e:
+        e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, 32)
+        assert idx[0].tolist() == list(range(32)) and idx[1].tolist() == list(range(32))
+        assert np.all(sc == 16.0)
