@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-gate", action="store_true")
+    ap.add_argument("--no-batched", action="store_true")
+    ap.add_argument("--no-int32", action="store_true")
     ap.add_argument("--schedule", type=int, default=None)
     ap.add_argument("--ctas-per-sm", type=int, default=None)
     ap.add_argument("--stage-bytes", type=int, default=None)
@@ -219,6 +221,81 @@ def run_reference(args):
     return 0
 
 
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def time_device(stream, fn, steps, warmup):
+    """Per-call device times (ms) of fn() on `stream`, events at call boundaries."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for j in range(steps):
+            ev[j].record(stream)
+            fn()
+        ev[steps].record(stream)
+    torch.cuda.synchronize()
+    return [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
+
+
+def run_batched(rbf, steps, warmup):
+    """Batched queries: B=256 x N=1,000,000 x D=768, bf16 corpus, fp32
+    accumulate, K=32 (tensor-core scoring + fused select + merge)."""
+    import torch
+    import workloads
+    n, d, b, k = 1_000_000, 768, 256, 32
+    c = workloads.unit_corpus(n, d, seed=1)
+    qs = workloads.unit_queries(b, d, seed=2)
+    workloads.plant_near_duplicates(c, qs, per_query=10, noise=0.05, seed=3)
+    st = torch.cuda.Stream()
+    e = rbf.Engine(n, d, k, max_batch=b, flags=rbf.RBF_FLAG_BF16_CORPUS, stream=st)
+    e.upload_corpus_rowmajor(c)
+    del c
+    dq = torch.from_numpy(qs).cuda()
+    di = torch.empty((b, k), dtype=torch.int32, device="cuda")
+    ds = torch.empty((b, k), dtype=torch.float32, device="cuda")
+    ms = time_device(st, lambda: e.search_resident_batch_dev(dq, k, di, ds), steps, warmup)
+    e.close()
+    p50 = percentile(ms, 50) * 1e-3
+    flops = 2.0 * b * n * d
+    peak, src = bf16_peak()
+    return {"workload": "B=256 x N=1,000,000 x D=768 bf16 corpus (fp32 accumulate), K=32, 10 planted rows/query",
+            "p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
+            "tflops": round(flops / p50 / 1e12, 1), "tensor_peak_tflops": peak, "peak_source": src,
+            "tensor_frac": round(flops / p50 / 1e12 / peak, 4),
+            "corpus_gbs": round(n * d * 2 / p50 / 1e9, 1), "queries_per_s": round(b / p50, 1),
+            "launches_per_call": 6, "steps": len(ms)}
+
+
+def run_int32(rbf, steps, warmup):
+    """Flat int32 two-stage top-K: 100,000,000 values, K=20 and K=50."""
+    import torch
+    import workloads
+    n = 100_000_000
+    x = torch.from_numpy(workloads.int32_uniform(n, seed=1)).cuda()
+    st = torch.cuda.Stream()
+    e = rbf.Engine(16, 16, 64, stream=st)
+    out = {"workload": "n=100,000,000 int32 uniform over the full range"}
+    dv = torch.empty(64, dtype=torch.int32, device="cuda")
+    dp = torch.empty(64, dtype=torch.int64, device="cuda")
+    for k in (20, 50):
+        ms = time_device(st, lambda: e.topk_int32_dev(x, k, dv, dp), steps, warmup)
+        p50 = percentile(ms, 50) * 1e-3
+        out[f"k{k}"] = {"p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
+                        "gbs": round(4.0 * n / p50 / 1e9, 1)}
+    e.close()
+    return out
+
+
 def percentile(xs, p):
     s = sorted(xs)
     if not s:
@@ -363,6 +440,10 @@ def main():
                 "traffic": ncu_traffic(), "bytes_per_launch": bytes_per_step,
                 "vs_8tbs": round(achieved / 8000.0, 4)}
 
+    eng.close()
+    batched = run_batched(rbf, 30, 3) if (rank == 0 and not args.no_batched) else None
+    int32 = run_int32(rbf, 50, 5) if (rank == 0 and not args.no_int32) else None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, cores, sample, _ = cpu_oracle_rate(c, qs, 8)
@@ -382,8 +463,11 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * args.steps, "clocks": clocks,
         }
+        if batched is not None:
+            line["batched"] = batched
+        if int32 is not None:
+            line["int32"] = int32
         print(json.dumps(line), flush=True)
-    eng.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
