@@ -28,6 +28,7 @@ constexpr int kResultHeader = 16;  // error word + padding, ahead of the results
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kI32CtasPerSm = 2;
 constexpr int64_t kSampleRows = 16384;  // rows of the batched path's threshold pre-pass
+constexpr int64_t kI32SampleElems = 65536;  // elements of the int32 path's threshold pre-pass
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -56,6 +57,7 @@ struct rbf_engine {
   void* corpus_bf16 = nullptr;   // max_n x max_pitch_bf16
   void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
+  uint64_t* i32_theta0 = nullptr;  // int32 path: K-th key over the element sample
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
@@ -234,6 +236,7 @@ void release(rbf_engine* e) {
   cudaFree(e->corpus_bf16);
   cudaFree(e->query_bf16);
   cudaFree(e->theta0);
+  cudaFree(e->i32_theta0);
   cudaFree(e->query);
   cudaFree(e->partials);
   cudaFree(e->errw);
@@ -324,6 +327,7 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->counters, 4 * sizeof(unsigned)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->i32_theta0, sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->result, e->result_bytes) == cudaSuccess;
   ok = ok && cudaMallocHost(&e->h_query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMallocHost(&e->h_result, e->result_bytes) == cudaSuccess;
@@ -567,17 +571,46 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
 static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* val,
                                      int64_t* pos, int* result_err) {
   const int64_t per_cta = 8192;  // below this many elements per CTA, use fewer CTAs
-  int64_t grid = std::min<int64_t>(int64_t(e->num_sms) * kI32CtasPerSm, (n + per_cta - 1) / per_cta);
-  grid = std::max<int64_t>(grid, 1);
-  if (static_cast<size_t>(grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
-  I32Launch a;
-  a.data = d_data;
-  a.n = n;
-  a.k = k;
-  a.partials = e->partials;
-  a.grid = static_cast<int>(grid);
-  RBF_LAUNCH(e, launch_topk_i32_stage1(a, e->stream));
-  return enqueue_merge(e, k, static_cast<int>(grid), 1, 1, val, pos, result_err);
+  auto stage1 = [&](int64_t count, const uint64_t* theta0, int* lists) -> rbf_status {
+    int64_t grid = std::min<int64_t>(int64_t(e->num_sms) * kI32CtasPerSm, (count + per_cta - 1) / per_cta);
+    grid = std::max<int64_t>(grid, 1);
+    if (static_cast<size_t>(grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+    I32Launch a;
+    a.data = d_data;
+    a.n = count;
+    a.k = k;
+    a.partials = e->partials;
+    a.grid = static_cast<int>(grid);
+    a.theta0 = theta0;
+    RBF_LAUNCH(e, launch_topk_i32_stage1(a, e->stream));
+    *lists = static_cast<int>(grid);
+    return RBF_OK;
+  };
+  // Sample bound: the exact K-th best key of the first kI32SampleElems
+  // elements is a lower bound on the final K-th key (they are part of the
+  // array), so the full pass drops every key below it from the start.
+  const uint64_t* theta0 = nullptr;
+  if (n >= 4 * kI32SampleElems) {
+    int lists = 0;
+    if (rbf_status st = stage1(kI32SampleElems, nullptr, &lists)) return st;
+    MergeLaunch m;
+    m.partials = e->partials;
+    m.lists = lists;
+    m.queries = 1;
+    m.k = k;
+    m.int_keys = 1;
+    m.out_a = val;  // overwritten by the final merge
+    m.out_b = pos;
+    m.err_call = nullptr;
+    m.err_sticky = nullptr;
+    m.result_err = nullptr;
+    m.kth_out = e->i32_theta0;
+    RBF_LAUNCH(e, launch_merge(m, e->stream));
+    theta0 = e->i32_theta0;
+  }
+  int lists = 0;
+  if (rbf_status st = stage1(n, theta0, &lists)) return st;
+  return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err);
 }
 
 static rbf_status check_i32_args(const rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k) {

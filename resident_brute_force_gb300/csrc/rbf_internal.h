@@ -62,6 +62,7 @@ struct I32Launch {
   int k;
   uint64_t* partials;        // grid lists of list_width(k) keys
   int grid;
+  const uint64_t* theta0 = nullptr;  // optional lower bound on the K-th key (keys >= it are kept)
 };
 cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
 

@@ -31,8 +31,8 @@ struct WarpBuffer {
 // Append the keys that beat theta (one candidate per lane, `pass` per lane)
 // to the warp buffer; merge 32 into the list whenever 32 or more are waiting.
 template <int R>
-__device__ __forceinline__ void offer(uint64_t (&v)[R], WarpBuffer& buf, int& cnt, uint64_t& theta, int k,
-                                      uint64_t key, bool pass, int lane) {
+__device__ __forceinline__ void offer(uint64_t (&v)[R], WarpBuffer& buf, int& cnt, uint64_t& theta, uint64_t floor_key,
+                                      int k, uint64_t key, bool pass, int lane) {
   const unsigned mask = __ballot_sync(kFullMask, pass);
   if (mask == 0) return;
   const int rank = __popc(mask & ((1u << lane) - 1u));
@@ -44,7 +44,7 @@ __device__ __forceinline__ void offer(uint64_t (&v)[R], WarpBuffer& buf, int& cn
     const uint64_t rest = buf.slot[32 + lane];
     __syncwarp();
     warp_list_insert32<R>(v, cand, lane);
-    theta = warp_list_get<R>(v, k - 1);
+    theta = umax64(warp_list_get<R>(v, k - 1), floor_key);
     cnt -= 32;
     if (lane < cnt) buf.slot[lane] = rest;
     __syncwarp();
@@ -53,7 +53,8 @@ __device__ __forceinline__ void offer(uint64_t (&v)[R], WarpBuffer& buf, int& cn
 
 template <int KP>
 __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t* __restrict__ data, int64_t n,
-                                                                  int k, uint64_t* partials) {
+                                                                  int k, uint64_t* partials,
+                                                                  const uint64_t* __restrict__ theta0) {
   constexpr int R = KP / 32;
   __shared__ WarpBuffer bufs[NW];
   __shared__ __align__(16) uint64_t lists[NW * KP];
@@ -72,7 +73,15 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
 
   uint64_t v[R];
   warp_list_clear<R>(v);
-  uint64_t theta = 0;
+  // theta: keys <= theta are dropped. With a lower bound b on the final K-th
+  // key (the K-th best key of a sample of the array), keys >= b can still
+  // make the top K, so theta starts at b - 1.
+  uint64_t floor_key = 0;
+  if (theta0) {
+    const uint64_t b0 = *theta0;
+    floor_key = b0 > 0 ? b0 - 1 : 0;
+  }
+  uint64_t theta = floor_key;
   int cnt = 0;
 
   const int64_t v0 = nvec * blockIdx.x / gridDim.x;
@@ -107,7 +116,7 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint64_t key = make_ikey(e[j], pos + j);
-        offer<R>(v, buf, cnt, theta, k, key, in && key > theta, lane);
+        offer<R>(v, buf, cnt, theta, floor_key, k, key, in && key > theta, lane);
       }
     }
   }
@@ -120,7 +129,7 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
       int64_t pos = 0;
       if (in) pos = (t < head) ? t : tail0 + (t - head);
       const uint64_t key = in ? make_ikey(data[pos], static_cast<uint32_t>(pos)) : 0;
-      offer<R>(v, buf, cnt, theta, k, key, in && key > theta, lane);
+      offer<R>(v, buf, cnt, theta, floor_key, k, key, in && key > theta, lane);
     }
   }
   // Flush what is left in the buffer (empty slots are the zero sentinel).
@@ -156,7 +165,7 @@ __global__ void wait_probe_kernel(int* err, uint64_t timeout_ns) {
 
 template <int KP>
 cudaError_t launch_t(const I32Launch& a, cudaStream_t stream) {
-  topk_i32_stage1_kernel<KP><<<a.grid, NW * 32, 0, stream>>>(a.data, a.n, a.k, a.partials);
+  topk_i32_stage1_kernel<KP><<<a.grid, NW * 32, 0, stream>>>(a.data, a.n, a.k, a.partials, a.theta0);
   return cudaGetLastError();
 }
 

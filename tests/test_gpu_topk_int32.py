@@ -98,3 +98,20 @@ def test_full_size_1e8(eng):
     for k in (20, 50):
         val, pos = eng.topk_int32(d, k)
         assert np.array_equal(pos, o_pos[:k]) and np.array_equal(val, o_val[:k])
+
+
+def test_sample_bound_cases(eng):
+    """n >= 262,144: the full pass starts from the K-th best key of the first
+    65,536 elements. Increasing arrays put every winner outside the sample;
+    constant arrays put them all inside it, tied with the bound."""
+    n = 600_000
+    cases = [
+        np.arange(n, dtype=np.int32),                                   # winners at the end
+        np.arange(n, 0, -1, dtype=np.int32),                            # winners at the start
+        np.full(n, 7, dtype=np.int32),                                  # every element ties
+        workloads.int32_small_range(n, seed=77, lo=-3, hi=3),           # heavy ties
+        np.where(np.arange(n) % 1000 == 999, np.int32(INT32_MAX), np.int32(INT32_MIN)).astype(np.int32),
+    ]
+    for x in cases:
+        for k in (1, 20, 50, 256):
+            _check(eng, _dev(x), x, k)
