@@ -70,7 +70,7 @@ struct rbf_engine {
   uint64_t* partials = nullptr;  // partials_cap keys
   size_t partials_cap = 0;
   int* errw = nullptr;           // [0] per call, [1] sticky, [2] self-test
-  unsigned* counters = nullptr;  // tile-claim counters of the dynamic schedule
+  unsigned* counters = nullptr;  // tile-claim counters: [0..1] scoring kernel, [2..3] int32 stream
   uint8_t* result = nullptr;     // device result block
   size_t result_bytes = 0;
 
@@ -609,7 +609,24 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
     theta0 = e->i32_theta0;
   }
   int lists = 0;
-  if (rbf_status st = stage1(n, theta0, &lists)) return st;
+  if (theta0) {
+    // Large arrays: the bulk-copy ring kernel, one CTA per SM.
+    I32StreamLaunch a;
+    a.data = d_data;
+    a.n = n;
+    a.k = k;
+    a.partials = e->partials;
+    a.theta0 = theta0;
+    a.counters = e->counters + 2;
+    a.err = e->errw;
+    a.grid = e->num_sms;
+    a.timeout_ns = e->timeout_ns;
+    if (static_cast<size_t>(a.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+    RBF_LAUNCH(e, launch_topk_i32_stream(a, e->stream));
+    lists = a.grid;
+  } else if (rbf_status st = stage1(n, nullptr, &lists)) {
+    return st;
+  }
   return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err);
 }
 

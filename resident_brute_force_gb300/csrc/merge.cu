@@ -6,15 +6,17 @@
 // (CUDA programming model series 9, section 3.1: one block over the GRID x K
 // stage-1 candidates).
 //
-// Each warp folds a strided subset of the lists into a register bitonic list
-// (reversed max + bitonic merge per list), loading the next list while it
-// merges the current one and reading only the first K entries of each list
-// (nothing past a list's K-th entry can reach the global top-K). The warp
+// The first K keys of every list (nothing past a list's K-th entry can reach
+// the global top-K) are staged in shared memory by all threads at once, one
+// round trip to L2; each warp then folds a strided subset of the staged lists
+// into a register bitonic list (reversed max + bitonic merge per list). The warp
 // lists are then merged pairwise in shared memory and warp 0 writes the best
 // K decoded. The keys already encode the ordering rule, so every comparison
 // is one unsigned 64-bit compare. The kernel is launched as a programmatic
 // dependent of the kernel that wrote the lists, so its launch overlaps that
 // kernel's tail; it waits for the lists before touching them.
+#include <algorithm>
+
 #include "rbf_device.cuh"
 #include "rbf_internal.h"
 
@@ -32,24 +34,15 @@ struct Params {
   int* err_sticky;
   int* result_err;
   uint64_t* kth_out;  // optional: the K-th key of each query
+  int stage_lists;    // lists staged in shared memory at a time
 };
-
-// List l's element KP-1-e for e = s*32 + lane, as the second operand of a
-// reversed-max fold; entries past the K-th read as the empty sentinel.
-template <int R>
-__device__ __forceinline__ void load_reversed(uint64_t (&dst)[R], const uint64_t* list, int k, int lane) {
-  constexpr int KP = 32 * R;
-#pragma unroll
-  for (int s = 0; s < R; ++s) {
-    const int e = KP - 1 - (s * 32 + lane);
-    dst[s] = (e < k) ? __ldcg(list + e) : 0ull;
-  }
-}
 
 template <int KP, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Params p) {
   constexpr int R = KP / 32;
-  extern __shared__ __align__(16) uint64_t lists[];
+  extern __shared__ __align__(16) uint64_t smem[];
+  uint64_t* lists = smem;                          // WARPS lists of KP keys (the tree)
+  uint64_t* stage = smem + WARPS * KP;             // staged list heads, k keys each
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   pdl_wait();
@@ -57,19 +50,29 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
 
   uint64_t v[R];
   warp_list_clear<R>(v);
-  uint64_t nxt[R];
-  int l = warp;
-  if (l < p.lists) load_reversed<R>(nxt, base + static_cast<size_t>(l) * KP, p.k, lane);
-  while (l < p.lists) {
-    uint64_t cur[R];
+  // Lists are staged in groups that fit the staging area: every thread loads
+  // its share of the group's first-k keys at once (one round trip to L2),
+  // then each warp folds a strided subset of the staged lists.
+  const int per_group = p.stage_lists;
+  for (int g0 = 0; g0 < p.lists; g0 += per_group) {
+    const int gl = min(per_group, p.lists - g0);
+    const int total = gl * p.k;
+    for (int i = threadIdx.x; i < total; i += WARPS * 32) {
+      const int l = i / p.k;
+      const int e = i - l * p.k;
+      stage[i] = __ldcg(base + static_cast<size_t>(g0 + l) * KP + e);
+    }
+    __syncthreads();
+    for (int l = warp; l < gl; l += WARPS) {
+      const uint64_t* src = stage + l * p.k;
 #pragma unroll
-    for (int s = 0; s < R; ++s) cur[s] = nxt[s];
-    const int ln = l + WARPS;
-    if (ln < p.lists) load_reversed<R>(nxt, base + static_cast<size_t>(ln) * KP, p.k, lane);
-#pragma unroll
-    for (int s = 0; s < R; ++s) v[s] = umax64(v[s], cur[s]);
-    warp_bitonic_merge_desc<R>(v, lane);
-    l = ln;
+      for (int s = 0; s < R; ++s) {
+        const int e = KP - 1 - (s * 32 + lane);
+        v[s] = umax64(v[s], e < p.k ? src[e] : 0ull);
+      }
+      warp_bitonic_merge_desc<R>(v, lane);
+    }
+    __syncthreads();
   }
   warp_list_store<R>(v, lists + warp * KP, lane);
   __syncthreads();
@@ -108,15 +111,19 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
   }
 }
 
+constexpr int kStageBytes = 160 * 1024;  // shared memory for staged list heads
+
 template <int KP, int WARPS>
-cudaError_t launch_t(const Params& p, int queries, cudaStream_t stream) {
+cudaError_t launch_t(Params p, int queries, cudaStream_t stream) {
   auto fn = merge_partials_kernel<KP, WARPS>;
-  const int smem = WARPS * KP * 8;
+  p.stage_lists = std::max(1, std::min(p.lists, kStageBytes / (8 * p.k)));
+  const int smem = WARPS * KP * 8 + p.stage_lists * p.k * 8;
   static int configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int want = WARPS * KP * 8 + kStageBytes;
+  if (want > configured) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
     if (e != cudaSuccess) return e;
-    configured = smem;
+    configured = want;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(queries));

@@ -66,6 +66,21 @@ struct I32Launch {
 };
 cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
 
+// Stage 1 for large arrays: bulk-copy ring, dynamic 64 KB tile claims, one
+// CTA of 8 consumer warps + 1 producer per SM.
+struct I32StreamLaunch {
+  const int32_t* data;
+  int64_t n;
+  int k;
+  uint64_t* partials;          // grid lists of list_width(k) keys
+  const uint64_t* theta0;      // optional lower bound on the K-th key
+  unsigned* counters;          // 2 words, zero between launches
+  int* err;
+  int grid;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream);
+
 cudaError_t launch_wait_probe(int* err, uint64_t timeout_ns, cudaStream_t stream);
 
 // Batched queries (tensor cores). K <= 32; each launch covers up to 256

@@ -51,6 +51,52 @@ __device__ __forceinline__ void offer(uint64_t (&v)[R], WarpBuffer& buf, int& cn
   }
 }
 
+// One step of 4 x int4 per lane (16 values, positions pos_base + 4*32*q + 4*lane
+// + j in the lane's view): a superset mask of the values that may beat theta
+// (value code >= theta's, settled exactly by the key compare), a warp vote,
+// and a walk over the union of flagged slots in which each lane offers the
+// value in that slot if it flagged it. Slot b = 4*q + j.
+template <int R>
+__device__ __forceinline__ void scan16(uint64_t (&v)[R], WarpBuffer& buf, int& cnt, uint64_t& theta,
+                                       uint64_t floor_key, int k, const int4 (&x)[4], const bool (&in)[4],
+                                       const uint32_t (&pos)[4], int lane) {
+  const uint32_t theta_hi = static_cast<uint32_t>(theta >> 32);
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (in[q]) {
+      m |= ((static_cast<uint32_t>(x[q].x) ^ 0x80000000u) >= theta_hi ? 1u : 0u) << (4 * q + 0);
+      m |= ((static_cast<uint32_t>(x[q].y) ^ 0x80000000u) >= theta_hi ? 1u : 0u) << (4 * q + 1);
+      m |= ((static_cast<uint32_t>(x[q].z) ^ 0x80000000u) >= theta_hi ? 1u : 0u) << (4 * q + 2);
+      m |= ((static_cast<uint32_t>(x[q].w) ^ 0x80000000u) >= theta_hi ? 1u : 0u) << (4 * q + 3);
+    }
+  }
+  uint32_t u = __reduce_or_sync(kFullMask, m);
+  while (u) {
+    const int b = __ffs(u) - 1;
+    u &= u - 1;
+    const int q = b >> 2;
+    int32_t val = 0;
+    // A uniform switch picks the register (dynamic indexing would spill).
+    switch (b) {
+#define RBF_SLOT(i, f) \
+  case i:              \
+    val = x[i / 4].f;  \
+    break;
+      RBF_SLOT(0, x) RBF_SLOT(1, y) RBF_SLOT(2, z) RBF_SLOT(3, w) RBF_SLOT(4, x) RBF_SLOT(5, y) RBF_SLOT(6, z)
+      RBF_SLOT(7, w) RBF_SLOT(8, x) RBF_SLOT(9, y) RBF_SLOT(10, z) RBF_SLOT(11, w) RBF_SLOT(12, x)
+      RBF_SLOT(13, y) RBF_SLOT(14, z) RBF_SLOT(15, w)
+#undef RBF_SLOT
+    }
+    uint32_t pq = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i == q) pq = pos[i];
+    const uint64_t key = make_ikey(val, pq + static_cast<uint32_t>(b & 3));
+    offer<R>(v, buf, cnt, theta, floor_key, k, key, ((m >> b) & 1u) && key > theta, lane);
+  }
+}
+
 template <int KP>
 __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t* __restrict__ data, int64_t n,
                                                                   int k, uint64_t* partials,
@@ -94,31 +140,15 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
       const int64_t i = c + u * 32 + lane;
       x[u] = (i < v1) ? __ldcs(vec + i) : make_int4(0, 0, 0, 0);
     }
-    // Cheap superset test first: a key can only beat theta if its value code
-    // is at least theta's. Most steps end here with one vote.
-    const uint32_t theta_hi = static_cast<uint32_t>(theta >> 32);
-    bool maybe = false;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const bool in = c + u * 32 + lane < v1;
-      maybe |= in && ((static_cast<uint32_t>(x[u].x) ^ 0x80000000u) >= theta_hi);
-      maybe |= in && ((static_cast<uint32_t>(x[u].y) ^ 0x80000000u) >= theta_hi);
-      maybe |= in && ((static_cast<uint32_t>(x[u].z) ^ 0x80000000u) >= theta_hi);
-      maybe |= in && ((static_cast<uint32_t>(x[u].w) ^ 0x80000000u) >= theta_hi);
-    }
-    if (!__any_sync(kFullMask, maybe)) continue;
+    bool in[kUnroll];
+    uint32_t pos[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = c + u * 32 + lane;
-      const bool in = i < v1;
-      const uint32_t pos = static_cast<uint32_t>(head + i * 4);
-      const int32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint64_t key = make_ikey(e[j], pos + j);
-        offer<R>(v, buf, cnt, theta, floor_key, k, key, in && key > theta, lane);
-      }
+      in[u] = i < v1;
+      pos[u] = static_cast<uint32_t>(head + i * 4);
     }
+    scan16<R>(v, buf, cnt, theta, floor_key, k, x, in, pos, lane);
   }
   if (blockIdx.x == 0 && warp == 0) {
     // Unaligned head and the tail: at most 3 + 3 elements.
@@ -151,6 +181,215 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
   if (warp == 0) warp_list_store<R>(v, partials + static_cast<size_t>(blockIdx.x) * KP, lane);
 }
 
+// Streaming variant for large arrays: the same per-warp selection, with the
+// 16-byte aligned body moved HBM -> shared memory by one-dimensional bulk
+// copies (TMA) into a 3-stage ring of 64 KB tiles claimed dynamically from a
+// global counter, so no registers are tied up by loads in flight. Eight
+// consumer warps scan each tile; one producer warp feeds the ring.
+constexpr int kSW = 8;                          // consumer warps
+constexpr int kSThreads = (kSW + 1) * 32;
+constexpr int kSStages = 3;
+constexpr int kSTileVec = 4096;                 // int4 per tile (64 KB)
+constexpr int kSTileBytes = kSTileVec * 16;
+
+struct StreamParams {
+  const int32_t* data;
+  int64_t n;
+  int k;
+  uint64_t* partials;
+  const uint64_t* theta0;
+  unsigned* counters;  // [0] tile claims, [1] finished CTAs; zero between launches
+  int* err;
+  uint64_t timeout_ns;
+};
+
+template <int KP>
+__global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const StreamParams p) {
+  constexpr int R = KP / 32;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSStages * kSTileBytes);
+  uint64_t* empty = full + kSStages;
+  int64_t* hdr_v0 = reinterpret_cast<int64_t*>(empty + kSStages);
+  int* hdr_nv = reinterpret_cast<int*>(hdr_v0 + kSStages);
+  WarpBuffer* bufs = reinterpret_cast<WarpBuffer*>(smem + kSStages * kSTileBytes + kSStages * 32);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(p.data);
+  int64_t head = static_cast<int64_t>(((16 - (addr & 15)) & 15) >> 2);
+  if (head > p.n) head = p.n;
+  const int64_t nvec = (p.n - head) >> 2;
+  const int64_t tail0 = head + nvec * 4;
+  const int4* vec = reinterpret_cast<const int4*>(p.data + head);
+  const int64_t total_tiles = (nvec + kSTileVec - 1) / kSTileVec;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kSStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  uint64_t v[R];
+  warp_list_clear<R>(v);
+
+  if (warp == kSW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int64_t claim = static_cast<int64_t>(atomicAdd(&p.counters[0], 1u));
+      int64_t issued = 0;
+      bool aborted = false;
+      for (int64_t i = 0;; ++i) {
+        const int s = static_cast<int>(i % kSStages);
+        const uint32_t u = static_cast<uint32_t>(i / kSStages);
+        const bool end = claim >= total_tiles;
+        int64_t v0 = 0;
+        int nv = 0;
+        if (!end) {
+          v0 = claim * kSTileVec;
+          nv = static_cast<int>(nvec - v0 < kSTileVec ? nvec - v0 : kSTileVec);
+          claim = static_cast<int64_t>(atomicAdd(&p.counters[0], 1u));
+        }
+        if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1u, p.timeout_ns)) {
+          atomicOr(p.err, kErrProducerTimeout);
+          aborted = true;
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+          aborted = true;
+          break;
+        }
+        if (end) {
+          hdr_nv[s] = -1;
+          mbar_arrive(&full[s]);
+          break;
+        }
+        hdr_v0[s] = v0;
+        hdr_nv[s] = nv;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nv) * 16u);
+        bulk_copy_g2s(ring + static_cast<size_t>(s) * kSTileBytes, vec + v0, static_cast<uint32_t>(nv) * 16u,
+                      &full[s], pol);
+        ++issued;
+      }
+      if (aborted) {
+        abort_flag = 1;
+        for (int64_t i = (issued > kSStages ? issued - kSStages : 0); i < issued; ++i) {
+          const int s = static_cast<int>(i % kSStages);
+          if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kSStages) & 1u, p.timeout_ns))
+            atomicOr(p.err, kErrDrainTimeout);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers
+    WarpBuffer& buf = bufs[warp];
+    uint64_t floor_key = 0;
+    if (p.theta0) {
+      const uint64_t b0 = *p.theta0;
+      floor_key = b0 > 0 ? b0 - 1 : 0;
+    }
+    uint64_t theta = floor_key;
+    int cnt = 0;
+    for (int64_t i = 0;; ++i) {
+      const int s = static_cast<int>(i % kSStages);
+      const uint32_t u = static_cast<uint32_t>(i / kSStages);
+      if (!__all_sync(kFullMask, mbar_wait(&full[s], u & 1u, p.timeout_ns))) {
+        if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
+        abort_flag = 1;
+        break;
+      }
+      const int nv = hdr_nv[s];
+      if (nv < 0 || *reinterpret_cast<volatile int*>(&abort_flag)) break;
+      const int64_t v0 = hdr_v0[s];
+      const int4* tile = reinterpret_cast<const int4*>(ring + static_cast<size_t>(s) * kSTileBytes);
+      // Each warp scans 4 x 32 consecutive int4 at a time (512 values).
+      for (int c = warp * 128; c < nv; c += kSW * 128) {
+        int4 x[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int t = c + q * 32 + lane;
+          x[q] = (t < nv) ? tile[t] : make_int4(INT32_MIN, INT32_MIN, INT32_MIN, INT32_MIN);
+        }
+        bool in[4];
+        uint32_t pos[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int t = c + q * 32 + lane;
+          in[q] = t < nv;
+          pos[q] = static_cast<uint32_t>(head + (v0 + t) * 4);
+        }
+        scan16<R>(v, buf, cnt, theta, floor_key, p.k, x, in, pos, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (blockIdx.x == 0 && warp == 0) {
+      // Unaligned head and the tail: at most 3 + 3 elements.
+      const int64_t extra = head + (p.n - tail0);
+      for (int64_t b = 0; b < extra; b += 32) {
+        const int64_t t = b + lane;
+        const bool in = t < extra;
+        int64_t pos = 0;
+        if (in) pos = (t < head) ? t : tail0 + (t - head);
+        const uint64_t key = in ? make_ikey(p.data[pos], static_cast<uint32_t>(pos)) : 0;
+        offer<R>(v, buf, cnt, theta, floor_key, p.k, key, in && key > theta, lane);
+      }
+    }
+    if (cnt > 0) {
+      const uint64_t cand = (lane < cnt) ? buf.slot[lane] : 0;
+      warp_list_insert32<R>(v, cand, lane);
+    }
+  }
+
+  // CTA merge of the consumer warps' lists (reusing the ring).
+  __syncthreads();
+  uint64_t* lists = reinterpret_cast<uint64_t*>(smem);
+  if (warp < kSW) warp_list_store<R>(v, lists + warp * KP, lane);
+  __syncthreads();
+#pragma unroll
+  for (int step = 1; step < kSW; step <<= 1) {
+    if (warp < kSW && (warp % (2 * step)) == 0 && warp + step < kSW) {
+      warp_list_merge_from<R>(v, lists + (warp + step) * KP, lane);
+      warp_list_store<R>(v, lists + warp * KP, lane);
+    }
+    __syncthreads();
+  }
+  if (warp == 0) warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(&p.counters[1], 1u);
+    if (done == gridDim.x - 1) {
+      atomicExch(&p.counters[0], 0u);
+      atomicExch(&p.counters[1], 0u);
+      __threadfence();
+    }
+  }
+}
+
+constexpr int kStreamSmem = kSStages * kSTileBytes + kSStages * 32 + kSW * static_cast<int>(sizeof(WarpBuffer));
+
+template <int KP>
+cudaError_t launch_stream_t(const StreamParams& p, int grid, cudaStream_t stream) {
+  auto fn = topk_i32_stream_kernel<KP>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  fn<<<grid, kSThreads, kStreamSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 // Wait on an mbarrier nothing ever arrives at, through the library's bounded
 // wait, and report the timeout. Exercises the timeout path without a fault.
 __global__ void wait_probe_kernel(int* err, uint64_t timeout_ns) {
@@ -177,6 +416,25 @@ cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream) {
     case 64: return launch_t<64>(a, stream);
     case 128: return launch_t<128>(a, stream);
     case 256: return launch_t<256>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream) {
+  StreamParams p;
+  p.data = a.data;
+  p.n = a.n;
+  p.k = a.k;
+  p.partials = a.partials;
+  p.theta0 = a.theta0;
+  p.counters = a.counters;
+  p.err = a.err;
+  p.timeout_ns = a.timeout_ns;
+  switch (list_width(a.k)) {
+    case 32: return launch_stream_t<32>(p, a.grid, stream);
+    case 64: return launch_stream_t<64>(p, a.grid, stream);
+    case 128: return launch_stream_t<128>(p, a.grid, stream);
+    case 256: return launch_stream_t<256>(p, a.grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
