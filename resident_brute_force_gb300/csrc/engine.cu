@@ -28,7 +28,9 @@ constexpr int kResultHeader = 16;  // error word + padding, ahead of the results
 constexpr int kMaxCtasPerSm = 4;
 constexpr int kI32CtasPerSm = 2;
 constexpr int64_t kSampleRows = 16384;  // rows of the batched path's threshold pre-pass
-constexpr int64_t kI32SampleElems = 65536;  // elements of the int32 path's threshold pre-pass
+constexpr int64_t kI32StreamMin = 262144;   // int32 arrays at least this long take the stream kernel
+constexpr int kI32SampleMinK = 65;          // from this K on, the stream kernel also gets a sample bound
+constexpr int64_t kI32SampleElems = 65536;  // elements of that sample
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -57,7 +59,6 @@ struct rbf_engine {
   void* corpus_bf16 = nullptr;   // max_n x max_pitch_bf16
   void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
-  uint64_t* i32_theta0 = nullptr;  // int32 path: K-th key over the element sample
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
@@ -68,6 +69,7 @@ struct rbf_engine {
   // Workspaces (device).
   float* query = nullptr;        // max_batch * max_pitch floats
   uint64_t* partials = nullptr;  // partials_cap keys
+  uint64_t* i32_theta0 = nullptr;  // int32 path: K-th key of the element sample
   size_t partials_cap = 0;
   int* errw = nullptr;           // [0] per call, [1] sticky, [2] self-test
   unsigned* counters = nullptr;  // tile-claim counters: [0..1] scoring kernel, [2..3] int32 stream
@@ -236,11 +238,11 @@ void release(rbf_engine* e) {
   cudaFree(e->corpus_bf16);
   cudaFree(e->query_bf16);
   cudaFree(e->theta0);
-  cudaFree(e->i32_theta0);
   cudaFree(e->query);
   cudaFree(e->partials);
   cudaFree(e->errw);
   cudaFree(e->counters);
+  cudaFree(e->i32_theta0);
   cudaFree(e->result);
   cudaFreeHost(e->h_query);
   cudaFreeHost(e->h_result);
@@ -326,7 +328,7 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->counters, 4 * sizeof(unsigned)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->counters, 8 * sizeof(unsigned)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->i32_theta0, sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->result, e->result_bytes) == cudaSuccess;
   ok = ok && cudaMallocHost(&e->h_query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
@@ -337,7 +339,7 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
     return RBF_ERR_OUT_OF_MEMORY;
   }
   ok = cudaMemsetAsync(e->errw, 0, 4 * sizeof(int), e->stream) == cudaSuccess &&
-       cudaMemsetAsync(e->counters, 0, 4 * sizeof(unsigned), e->stream) == cudaSuccess &&
+       cudaMemsetAsync(e->counters, 0, 8 * sizeof(unsigned), e->stream) == cudaSuccess &&
        cudaMemsetAsync(e->query, 0, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float), e->stream) ==
            cudaSuccess &&
        cudaStreamSynchronize(e->stream) == cudaSuccess;
@@ -570,8 +572,10 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
 
 static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* val,
                                      int64_t* pos, int* result_err) {
-  const int64_t per_cta = 8192;  // below this many elements per CTA, use fewer CTAs
-  auto stage1 = [&](int64_t count, const uint64_t* theta0, int* lists) -> rbf_status {
+  // Register-load stage 1 over contiguous ranges; below 8,192 elements per
+  // CTA fewer CTAs are used.
+  auto stage1 = [&](int64_t count, int* lists) -> rbf_status {
+    const int64_t per_cta = 8192;
     int64_t grid = std::min<int64_t>(int64_t(e->num_sms) * kI32CtasPerSm, (count + per_cta - 1) / per_cta);
     grid = std::max<int64_t>(grid, 1);
     if (static_cast<size_t>(grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
@@ -581,21 +585,28 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
     a.k = k;
     a.partials = e->partials;
     a.grid = static_cast<int>(grid);
-    a.theta0 = theta0;
     RBF_LAUNCH(e, launch_topk_i32_stage1(a, e->stream));
     *lists = static_cast<int>(grid);
     return RBF_OK;
   };
-  // Sample bound: the exact K-th best key of the first kI32SampleElems
-  // elements is a lower bound on the final K-th key (they are part of the
-  // array), so the full pass drops every key below it from the start.
+  int lists = 0;
+  if (n < kI32StreamMin) {
+    if (rbf_status st = stage1(n, &lists)) return st;
+    return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err);
+  }
+  // Large arrays: the bulk-copy ring kernel, one CTA per SM. Each CTA bounds
+  // the K-th key from its own slice before its first tile. That bound weakens
+  // as K grows (it comes from 16,384 values), so for K >= kI32SampleMinK the
+  // exact K-th key of the first kI32SampleElems elements -- also a lower
+  // bound, as they are part of the array -- is computed first and passed in.
+  if (static_cast<size_t>(e->num_sms) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
   const uint64_t* theta0 = nullptr;
-  if (n >= 4 * kI32SampleElems) {
-    int lists = 0;
-    if (rbf_status st = stage1(kI32SampleElems, nullptr, &lists)) return st;
+  if (k >= kI32SampleMinK) {
+    int sample_lists = 0;
+    if (rbf_status st = stage1(kI32SampleElems, &sample_lists)) return st;
     MergeLaunch m;
     m.partials = e->partials;
-    m.lists = lists;
+    m.lists = sample_lists;
     m.queries = 1;
     m.k = k;
     m.int_keys = 1;
@@ -608,25 +619,18 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
     RBF_LAUNCH(e, launch_merge(m, e->stream));
     theta0 = e->i32_theta0;
   }
-  int lists = 0;
-  if (theta0) {
-    // Large arrays: the bulk-copy ring kernel, one CTA per SM.
-    I32StreamLaunch a;
-    a.data = d_data;
-    a.n = n;
-    a.k = k;
-    a.partials = e->partials;
-    a.theta0 = theta0;
-    a.counters = e->counters + 2;
-    a.err = e->errw;
-    a.grid = e->num_sms;
-    a.timeout_ns = e->timeout_ns;
-    if (static_cast<size_t>(a.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
-    RBF_LAUNCH(e, launch_topk_i32_stream(a, e->stream));
-    lists = a.grid;
-  } else if (rbf_status st = stage1(n, nullptr, &lists)) {
-    return st;
-  }
+  I32StreamLaunch a;
+  a.data = d_data;
+  a.n = n;
+  a.k = k;
+  a.partials = e->partials;
+  a.theta0 = theta0;
+  a.counters = e->counters + 2;
+  a.err = e->errw;
+  a.grid = e->num_sms;
+  a.timeout_ns = e->timeout_ns;
+  RBF_LAUNCH(e, launch_topk_i32_stream(a, e->stream));
+  lists = e->num_sms;
   return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err);
 }
 

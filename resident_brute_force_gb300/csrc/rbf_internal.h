@@ -67,13 +67,14 @@ struct I32Launch {
 cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
 
 // Stage 1 for large arrays: bulk-copy ring, dynamic 64 KB tile claims, one
-// CTA of 8 consumer warps + 1 producer per SM.
+// CTA of 16 consumer warps + 1 producer per SM; each CTA bounds the K-th key
+// from its own 16,384-value slice before its first tile. K <= 256.
 struct I32StreamLaunch {
   const int32_t* data;
   int64_t n;
   int k;
   uint64_t* partials;          // grid lists of list_width(k) keys
-  const uint64_t* theta0;      // optional lower bound on the K-th key
+  const uint64_t* theta0;      // optional lower bound on the K-th key (keys >= it are kept)
   unsigned* counters;          // 2 words, zero between launches
   int* err;
   int grid;

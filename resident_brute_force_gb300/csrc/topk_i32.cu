@@ -184,24 +184,37 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
 // Streaming variant for large arrays: the same per-warp selection, with the
 // 16-byte aligned body moved HBM -> shared memory by one-dimensional bulk
 // copies (TMA) into a 3-stage ring of 64 KB tiles claimed dynamically from a
-// global counter, so no registers are tied up by loads in flight. Eight
+// global counter, so no registers are tied up by loads in flight. Sixteen
 // consumer warps scan each tile; one producer warp feeds the ring.
-constexpr int kSW = 8;                          // consumer warps
+//
+// Before the first tile each CTA takes a lower bound on the final K-th key
+// from its own slice of 16,384 values: the K-th largest of 256 group maxima
+// (groups of 64 values). K distinct groups each hold a key at least that
+// large, so at least K keys of the array are >= it and no key below it can be
+// in the top K. The consumers read the slice while the producer fills the
+// ring, and every key below the bound is dropped from the start. No CTA ever
+// waits for another.
+constexpr int kSW = 16;                         // consumer warps
 constexpr int kSThreads = (kSW + 1) * 32;
 constexpr int kSStages = 3;
 constexpr int kSTileVec = 4096;                 // int4 per tile (64 KB)
 constexpr int kSTileBytes = kSTileVec * 16;
+constexpr int kBoundGroups = 256;               // group maxima per slice (K <= 256)
+constexpr int kBoundVecPerThread = kSTileVec / (kSW * 32);  // 8 int4 = 32 values per thread
+static_assert(kSW * 32 == 2 * kBoundGroups, "two consumer threads per group");
 
 struct StreamParams {
   const int32_t* data;
   int64_t n;
   int k;
   uint64_t* partials;
-  const uint64_t* theta0;
+  const uint64_t* theta0;  // optional: a lower bound on the K-th key (keys >= it are kept)
   unsigned* counters;  // [0] tile claims, [1] finished CTAs; zero between launches
   int* err;
   uint64_t timeout_ns;
 };
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kSW * 32) : "memory"); }
 
 template <int KP>
 __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const StreamParams p) {
@@ -214,6 +227,7 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
   int* hdr_nv = reinterpret_cast<int*>(hdr_v0 + kSStages);
   WarpBuffer* bufs = reinterpret_cast<WarpBuffer*>(smem + kSStages * kSTileBytes + kSStages * 32);
   __shared__ int abort_flag;
+  __shared__ uint64_t s_bound;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -229,6 +243,7 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    s_bound = 0;
     for (int s = 0; s < kSStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSW);
@@ -296,6 +311,42 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     if (p.theta0) {
       const uint64_t b0 = *p.theta0;
       floor_key = b0 > 0 ? b0 - 1 : 0;
+    }
+    const int64_t slice = static_cast<int64_t>(blockIdx.x) * kSTileVec;
+    if (slice + kSTileVec <= nvec) {  // CTA-uniform: every consumer warp takes part
+      // Group g = threadIdx.x / 2 covers 16 vectors of the slice, 8 per thread,
+      // strided by 512 vectors so that every load is coalesced.
+      int4 x[kBoundVecPerThread];
+#pragma unroll
+      for (int j = 0; j < kBoundVecPerThread; ++j) x[j] = __ldcg(vec + slice + threadIdx.x + j * (kSW * 32));
+      uint64_t best = 0;
+#pragma unroll
+      for (int j = 0; j < kBoundVecPerThread; ++j) {
+        const uint32_t p0 = static_cast<uint32_t>(head + (slice + threadIdx.x + j * (kSW * 32)) * 4);
+        best = umax64(best, make_ikey(x[j].x, p0));
+        best = umax64(best, make_ikey(x[j].y, p0 + 1));
+        best = umax64(best, make_ikey(x[j].z, p0 + 2));
+        best = umax64(best, make_ikey(x[j].w, p0 + 3));
+      }
+      best = umax64(best, shfl_xor_u64(best, 1));
+      uint64_t* gmax = reinterpret_cast<uint64_t*>(bufs);  // 256 keys, 2 KB
+      if ((threadIdx.x & 1) == 0) gmax[threadIdx.x >> 1] = best;
+      consumer_bar();
+      // The K-th largest group maximum is the one with exactly K-1 larger
+      // (keys are distinct); each of the pair counts over half of the groups.
+      const int h = threadIdx.x & 1;
+      const ulonglong2* half = reinterpret_cast<const ulonglong2*>(gmax + h * (kBoundGroups / 2));
+      int greater = 0;
+#pragma unroll 8
+      for (int j = 0; j < kBoundGroups / 4; ++j) {
+        const ulonglong2 g = half[j];
+        greater += (g.x > best ? 1 : 0) + (g.y > best ? 1 : 0);
+      }
+      greater += __shfl_xor_sync(kFullMask, greater, 1);
+      if (h == 0 && greater == p.k - 1) s_bound = best;
+      consumer_bar();  // also: every read of gmax is done before the buffers are reused
+      const uint64_t b0 = s_bound;
+      if (b0 > 1) floor_key = umax64(floor_key, b0 - 1);
     }
     uint64_t theta = floor_key;
     int cnt = 0;
@@ -430,6 +481,7 @@ cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream
   p.counters = a.counters;
   p.err = a.err;
   p.timeout_ns = a.timeout_ns;
+  if (a.k < 1 || a.k > kBoundGroups) return cudaErrorInvalidValue;
   switch (list_width(a.k)) {
     case 32: return launch_stream_t<32>(p, a.grid, stream);
     case 64: return launch_stream_t<64>(p, a.grid, stream);

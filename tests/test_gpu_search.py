@@ -150,6 +150,7 @@ def test_device_entry_points_match_host(rbf):
     {"RBF_OPT_STAGE_BYTES": 8192},
     {"RBF_OPT_STAGE_BYTES": 65536, "RBF_OPT_SCHEDULE": 1},
     {"RBF_OPT_CTAS_PER_SM": 3, "RBF_OPT_SCHEDULE": 1},
+    {"RBF_OPT_CTAS_PER_SM": 4},      # more than 512 lists: the merge takes its general path
 ])
 def test_launch_shapes_same_result(rbf, opts):
     n, d = 30001, 1024

@@ -101,9 +101,10 @@ def test_full_size_1e8(eng):
 
 
 def test_sample_bound_cases(eng):
-    """n >= 262,144: the full pass starts from the K-th best key of the first
-    65,536 elements. Increasing arrays put every winner outside the sample;
-    constant arrays put them all inside it, tied with the bound."""
+    """n >= 262,144: CTA b starts from a lower bound on the K-th key taken
+    from its own slice of 16,384 values (vectors 4096 b .. 4096 b + 4095 of
+    the 16-byte aligned body). Increasing arrays put every winner outside the
+    early slices; constant arrays tie every key with the bound."""
     n = 600_000
     cases = [
         np.arange(n, dtype=np.int32),                                   # winners at the end
@@ -115,3 +116,19 @@ def test_sample_bound_cases(eng):
     for x in cases:
         for k in (1, 20, 50, 256):
             _check(eng, _dev(x), x, k)
+
+
+@pytest.mark.parametrize("offset", [0, 3])
+def test_winners_inside_one_slice(eng, offset):
+    """Every winner lies in one CTA's bound slice (slice 7), at random
+    positions, with ties among them: that slice's bound is the exact K-th of
+    its group maxima, the other slices' bounds are far below it."""
+    n = 1_000_003
+    rng = np.random.default_rng(8)
+    x = workloads.int32_small_range(n + offset, seed=9, lo=-1000, hi=1000)
+    lo = offset + ((16 - (offset * 4) % 16) % 16) // 4 + 7 * 16384
+    hot = lo + rng.choice(16384, size=600, replace=False)
+    x[hot] = INT32_MAX - rng.integers(0, 40, size=600).astype(np.int32)
+    d = _dev(x)[offset:]
+    for k in (1, 20, 50, 256):
+        _check(eng, d, x[offset:], k)
