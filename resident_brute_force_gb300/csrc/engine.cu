@@ -56,7 +56,7 @@ struct rbf_engine {
   bool ready = false;
 
   // bf16 copies for the batched path (RBF_FLAG_BF16_CORPUS).
-  void* corpus_bf16 = nullptr;   // max_n x max_pitch_bf16
+  void* corpus_bf16 = nullptr;   // tile-major, max_n rounded up to 128 rows x max_pitch_bf16
   void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
   int max_pitch_bf16 = 0;
@@ -321,7 +321,8 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   if (flags & RBF_FLAG_FP32_CORPUS)
     ok = ok && cudaMalloc(&e->corpus, static_cast<size_t>(max_n) * e->max_pitch * sizeof(float)) == cudaSuccess;
   if (flags & RBF_FLAG_BF16_CORPUS) {
-    ok = ok && cudaMalloc(&e->corpus_bf16, static_cast<size_t>(max_n) * e->max_pitch_bf16 * 2) == cudaSuccess;
+    ok = ok && cudaMalloc(&e->corpus_bf16, align_up(static_cast<size_t>(max_n), 128) * e->max_pitch_bf16 * 2) ==
+                   cudaSuccess;
     ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
     ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
   }
@@ -419,8 +420,8 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
   }
   if (e->corpus_bf16) {
     const int pb = static_cast<int>(align_up(static_cast<size_t>(d), kBf16PitchAlign));
-    RBF_LAUNCH(e, launch_to_bf16(e->corpus, pitch, e->corpus_bf16, pb, n, n, d, e->num_sms, e->stream));
-    if (!make_bf16_tensor_map(&e->tmap_corpus, e->corpus_bf16, n, pb) ||
+    RBF_LAUNCH(e, launch_to_bf16_tiled(e->corpus, pitch, e->corpus_bf16, n, pb, d, e->num_sms, e->stream));
+    if (!make_bf16_tiled_tensor_map(&e->tmap_corpus, e->corpus_bf16, n, pb) ||
         !make_bf16_tensor_map(&e->tmap_query, e->query_bf16, e->query_rows, pb)) {
       e->tmaps_ready = false;
       return RBF_ERR_CUDA;

@@ -11,7 +11,9 @@
 // One CTA per SM, 10 warps:
 //   warp 0     TMA producer: per 64-wide K chunk, the query tile(s) (up to
 //              256 queries = two 128-row M tiles) and 128 corpus rows, 128-byte
-//              swizzled, into a 4-stage shared-memory ring;
+//              swizzled, into a 4-stage shared-memory ring. The bf16 corpus is
+//              stored tile-major ([row tile][K chunk][128 rows][64]), so each
+//              corpus load is one contiguous 16 KB block of HBM;
 //   warp 1     TMEM owner and MMA issuer: one thread issues
 //              tcgen05.mma.cta_group::1.kind::f16 (M = 128 queries, N = 128
 //              corpus rows, K = 16) into one of two accumulator buffers, so the
@@ -98,6 +100,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Three-dimensional tiled TMA load (x, y within a 16 KB block, z = block).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
 
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], bytes);
           tma_load_2d(st, &tmap_q, kc * kKChunk, p.q_row0, &full[s], pol_q);
           if (p.num_mt > 1) tma_load_2d(st + kSubTileBytes, &tmap_q, kc * kKChunk, p.q_row0 + 128, &full[s], pol_q);
-          tma_load_2d(st + 2 * kSubTileBytes, &tmap_c, kc * kKChunk, t * kTileRows, &full[s], pol_c);
+          tma_load_3d(st + 2 * kSubTileBytes, &tmap_c, 0, 0, t * p.kchunks + kc, &full[s], pol_c);
         }
       }
       if (aborted) {
@@ -490,6 +502,25 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, int64_t src_pitch,
   }
 }
 
+// fp32 [rows][src_pitch] -> bf16 tile-major [tiles][kchunks][128][64], zero
+// past `cols` and for rows in [rows, tiles * 128).
+__global__ void to_bf16_tiled_kernel(const float* __restrict__ src, int64_t src_pitch,
+                                     __nv_bfloat16* __restrict__ dst, int64_t rows, int64_t tiles, int kchunks,
+                                     int cols) {
+  const int64_t total = tiles * kchunks * (kTileRows * kKChunk);
+  for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
+       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int cc = static_cast<int>(o % kKChunk);
+    const int rr = static_cast<int>((o / kKChunk) % kTileRows);
+    const int64_t tk = o / (kTileRows * kKChunk);
+    const int kc = static_cast<int>(tk % kchunks);
+    const int64_t r = (tk / kchunks) * kTileRows + rr;
+    const int c = kc * kKChunk + cc;
+    const float v = (r < rows && c < cols) ? src[r * src_pitch + c] : 0.0f;
+    dst[o] = __float2bfloat16_rn(v);
+  }
+}
+
 }  // namespace
 
 int gemm_select_smem_bytes() {
@@ -507,6 +538,34 @@ bool make_bf16_tensor_map(void* map_out, const void* base, int64_t rows, int pit
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_bf16_tiled_tensor_map(void* map_out, const void* base, int64_t rows, int pitch_elems) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int64_t blocks = (rows + kTileRows - 1) / kTileRows * (pitch_elems / kKChunk);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKChunk), static_cast<cuuint64_t>(kTileRows),
+                              static_cast<cuuint64_t>(blocks)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kKChunk) * 2, static_cast<cuuint64_t>(kSubTileBytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKChunk), static_cast<cuuint32_t>(kTileRows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_to_bf16_tiled(const float* src, int64_t src_pitch, void* dst, int64_t rows, int pitch_elems,
+                                 int cols, int num_sms, cudaStream_t st) {
+  const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
+  const int kchunks = pitch_elems / kKChunk;
+  const int64_t total = tiles * kchunks * (kTileRows * kKChunk);
+  int64_t blocks = (total + 255) / 256;
+  blocks = blocks < int64_t(num_sms) * 8 ? blocks : int64_t(num_sms) * 8;
+  if (blocks < 1) blocks = 1;
+  to_bf16_tiled_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, static_cast<__nv_bfloat16*>(dst),
+                                                                rows, tiles, kchunks, cols);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,

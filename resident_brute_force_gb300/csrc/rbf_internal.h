@@ -109,6 +109,11 @@ struct GemmSelectLaunch {
 int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
 bool make_bf16_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);
+// Corpus copy for the batched path, tile-major: [ceil(rows/128)][pitch/64][128][64]
+// bf16, rows past `rows` zero. The map's box is one 16 KB block.
+bool make_bf16_tiled_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);
+cudaError_t launch_to_bf16_tiled(const float* src, int64_t src_pitch, void* dst, int64_t rows, int pitch_elems,
+                                 int cols, int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream);
 // fp32 [rows][src_pitch] -> bf16 [rows_total][dst_pitch] (RN-even), zero padded.
 cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,
