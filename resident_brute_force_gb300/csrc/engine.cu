@@ -492,7 +492,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
                                e->stream));
   // The scoring + select kernel over rows [0, rows): one launch per group of
   // up to 256 queries; returns the number of per-CTA lists per query.
-  auto score_groups = [&](int64_t rows, const uint64_t* theta0, int* lists) -> rbf_status {
+  auto score_groups = [&](int64_t rows, int bound_mode, const uint64_t* theta0, int* lists) -> rbf_status {
     const int64_t tiles = (rows + 127) / 128;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles, e->num_sms)));
     if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;
@@ -511,18 +511,21 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
       a.grid = grid;
       a.timeout_ns = e->timeout_ns;
       a.theta0 = theta0;
+      a.bound_mode = bound_mode;
       RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
     }
     *lists = grid;
     return RBF_OK;
   };
-  // Pre-pass: the exact K-th best key of every query over the first
-  // kSampleRows rows. It is a lower bound on the final K-th key (those rows
-  // are part of the corpus), so the main pass drops every key below it.
+  // Pre-pass over the first kSampleRows rows (one 128-row tile per CTA):
+  // no selection, each CTA keeps per query the best key of every 32-row
+  // chunk, and the merge takes the K-th largest of those 512 chunk maxima.
+  // K distinct rows score at least that much, so it is a lower bound on the
+  // final K-th key, and the main pass drops every key below it.
   const uint64_t* theta0 = nullptr;
-  if (e->n >= 4 * kSampleRows) {
+  if (e->n >= 4 * kSampleRows && kSampleRows / 128 <= e->num_sms) {
     int lists = 0;
-    if (rbf_status st = score_groups(kSampleRows, nullptr, &lists)) return st;
+    if (rbf_status st = score_groups(kSampleRows, 1, nullptr, &lists)) return st;
     MergeLaunch m;
     m.partials = e->partials;
     m.lists = lists;
@@ -539,7 +542,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     theta0 = e->theta0;
   }
   int grid = 0;
-  if (rbf_status st = score_groups(e->n, theta0, &grid)) return st;
+  if (rbf_status st = score_groups(e->n, 0, theta0, &grid)) return st;
   return enqueue_merge(e, k, grid, b, 0, d_idx, d_score, result_err);
 }
 

@@ -93,6 +93,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane, waited for.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Two-dimensional tiled TMA load (x = element offset along the row, y = row).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                             uint64_t policy) {
@@ -221,6 +235,7 @@ struct Params {
   int k;
   uint64_t timeout_ns;
   const uint64_t* theta0;  // optional per-query lower bound on the K-th key
+  int bound_mode;          // 1: write the best key of each 32-row chunk instead of a top-K list
 };
 
 template <int KP>
@@ -396,7 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
     };
 
-    if (m < p.num_mt) {
+    if (m < p.num_mt && p.bound_mode) {
+      // Bound mode: per query, the best key of each 32-row chunk. Any K of
+      // these belong to K distinct rows, so the K-th largest of them over all
+      // CTAs is a lower bound on the query's K-th key. At most 4 per tile are
+      // kept (one CTA scores one tile here); they are written best first.
+      uint64_t best[4] = {0ull, 0ull, 0ull, 0ull};
       int tile_i = 0;
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
         const int b = tile_i & 1;
@@ -408,39 +428,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) break;
         tc_fence_after();
         const int64_t row0 = static_cast<int64_t>(t) * kTileRows;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < kTileRows / 32; ++c) {
           float sc[32];
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                  static_cast<uint32_t>(b * 256 + m * 128 + c * 32);
           tmem_ld32(taddr, sc);
           const int64_t rb = row0 + c * 32;
-          // One bit per column whose score may beat theta (a superset test:
-          // ties are settled below by the key compare), built without
-          // branches; rows past the corpus end are masked off.
-          uint32_t m = 0;
+          uint64_t top = 0;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
-          if (filling) m = 0xFFFFFFFFu;
-          if (p.n - rb < 32) m &= (p.n - rb > 0) ? ((1u << (p.n - rb)) - 1u) : 0u;
-          // Walk the columns any lane flagged, in order, warp-uniformly.
-          uint32_t u = __reduce_or_sync(kFullMask, m);
-          while (u) {
-            const int j = __ffs(u) - 1;
-            u &= u - 1;
-            if (m & (1u << j)) {
-              const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j));
-              if (key > theta) {
-                cand[cnt * 256 + slot] = key;
-                ++cnt;
-              }
-            }
-            if (__any_sync(kFullMask, cnt == kCandCap)) merge_buffer();
+          for (int j = 0; j < 32; ++j) {
+            const uint64_t key = (rb + j < p.n) ? make_key(sc[j], static_cast<uint32_t>(rb + j)) : 0ull;
+            top = umax64(top, key);
           }
+          best[c] = umax64(best[c], top);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
+      }
+      // Best first: a 4-key sorting network.
+      auto cswap = [](uint64_t& x, uint64_t& y) {
+        const uint64_t hi = umax64(x, y), lo = umin64(x, y);
+        x = hi;
+        y = lo;
+      };
+      cswap(best[0], best[1]);
+      cswap(best[2], best[3]);
+      cswap(best[0], best[2]);
+      cswap(best[1], best[3]);
+      cswap(best[1], best[2]);
+      if (qlocal < p.q_count) {
+        uint64_t* dst = p.partials + (static_cast<size_t>(p.q_out0 + qlocal) * gridDim.x + blockIdx.x) * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = best[i];
+#pragma unroll
+        for (int i = 4; i < 32; ++i) dst[i] = 0ull;
+      }
+    } else if (m < p.num_mt) {
+      int tile_i = 0;
+      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
+        const int b = tile_i & 1;
+        if (!__all_sync(kFullMask, mbar_wait(&acc_full[b], static_cast<uint32_t>(tile_i >> 1) & 1u, p.timeout_ns))) {
+          if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
+          abort_flag = 1;
+          break;
+        }
+        if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) break;
+        tc_fence_after();
+        const int64_t row0 = static_cast<int64_t>(t) * kTileRows;
+        // Two 64-column TMEM loads per tile; the accumulator buffer is handed
+        // back to the MMA warp as soon as the second one has landed, before
+        // its columns are examined.
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(b * 256 + m * 128);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float s64[64];
+          tmem_ld64(tbase + static_cast<uint32_t>(h * 64), s64);
+          if (h == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+          }
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const float(&sc)[32] = *reinterpret_cast<const float(*)[32]>(&s64[c2 * 32]);
+            const int64_t rb = row0 + h * 64 + c2 * 32;
+            // One bit per column whose score may beat theta (a superset test:
+            // ties are settled below by the key compare), built without
+            // branches; rows past the corpus end are masked off.
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
+            if (filling) m = 0xFFFFFFFFu;
+            if (p.n - rb < 32) m &= (p.n - rb > 0) ? ((1u << (p.n - rb)) - 1u) : 0u;
+            // Walk the columns any lane flagged, in order, warp-uniformly.
+            uint32_t u = __reduce_or_sync(kFullMask, m);
+            while (u) {
+              const int j = __ffs(u) - 1;
+              u &= u - 1;
+              if (m & (1u << j)) {
+                const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j));
+                if (key > theta) {
+                  cand[cnt * 256 + slot] = key;
+                  ++cnt;
+                }
+              }
+              if (__any_sync(kFullMask, cnt == kCandCap)) merge_buffer();
+            }
+          }
+        }
       }
       if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
       if (qlocal < p.q_count) {
@@ -593,6 +671,13 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.k = a.k;
   p.timeout_ns = a.timeout_ns;
   p.theta0 = a.theta0;
+  p.bound_mode = a.bound_mode;
+  if (a.bound_mode) {
+    // Bound mode writes 4 keys per tile and query: one tile per CTA.
+    if (p.num_tiles > a.grid) return cudaErrorInvalidValue;
+    return launch_t<8>(*static_cast<const CUtensorMap*>(a.tmap_q), *static_cast<const CUtensorMap*>(a.tmap_c), p,
+                       a.grid, stream);
+  }
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
   if (a.k <= 8) return launch_t<8>(tq, tc, p, a.grid, stream);

@@ -51,6 +51,7 @@ struct Params {
 };
 
 constexpr int kSurvivorCap = 2048;        // keys gathered by the fast path
+constexpr int kManyQueries = 64;          // from this many queries on, merge CTAs are 8 warps
 constexpr int kFastMaxLists = 512;        // lists the bound selection handles (its work grows as lists^2)
 constexpr int kStageBytes = 160 * 1024;   // shared memory for staged list heads
 
@@ -296,6 +297,17 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
   p.kth_out = a.kth_out;
+  // One query: a wide CTA to shorten the single merge. Many queries: 8-warp
+  // CTAs, so that several fit on each SM and all queries run in one wave.
+  if (a.queries >= kManyQueries) {
+    switch (list_width(a.k)) {
+      case 32: return launch_t<32, 8>(p, a.queries, stream);
+      case 64: return launch_t<64, 8>(p, a.queries, stream);
+      case 128: return launch_t<128, 8>(p, a.queries, stream);
+      case 256: return launch_t<256, 8>(p, a.queries, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (list_width(a.k)) {
     case 32: return launch_t<32, 32>(p, a.queries, stream);
     case 64: return launch_t<64, 32>(p, a.queries, stream);

@@ -105,6 +105,8 @@ struct GemmSelectLaunch {
   int grid;
   uint64_t timeout_ns;
   const uint64_t* theta0;    // optional per-query lower bound on the K-th key (keys >= it are kept)
+  int bound_mode = 0;        // 1: no selection; each CTA writes, per query, the best key of every
+                             // 32-row chunk it scored (at most 4 per tile, best first, then zeros)
 };
 int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
