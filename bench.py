@@ -73,8 +73,9 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the files that define the scoring kernel's code."""
     h = hashlib.sha256()
-    for f in ("score_select.cu", "rbf_device.cuh", "rbf_internal.h"):
+    for f in ("score_select.cu", "rbf_device.cuh"):
         with open(os.path.join(ROOT, "resident_brute_force_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
