@@ -269,12 +269,19 @@ def run_batched(rbf, steps, warmup):
     p50 = percentile(ms, 50) * 1e-3
     flops = 2.0 * b * n * d
     peak, src = bf16_peak()
+    hbm, hsrc = hbm_peak()
+    corpus_bytes = n * d * 2
+    # Both rooflines: the tensor work at the bf16 peak and the one pass over
+    # the bf16 corpus at the HBM peak; the slower of the two bounds the call.
+    bound = "hbm" if corpus_bytes / (hbm * 1e9) > flops / (peak * 1e12) else "tensor"
     return {"workload": "B=256 x N=1,000,000 x D=768 bf16 corpus (fp32 accumulate), K=32, 10 planted rows/query",
             "p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
             "tflops": round(flops / p50 / 1e12, 1), "tensor_peak_tflops": peak, "peak_source": src,
             "tensor_frac": round(flops / p50 / 1e12 / peak, 4),
-            "corpus_gbs": round(n * d * 2 / p50 / 1e9, 1), "queries_per_s": round(b / p50, 1),
-            "launches_per_call": 6, "steps": len(ms)}
+            "corpus_gbs": round(corpus_bytes / p50 / 1e9, 1), "hbm_peak_gbs": hbm, "hbm_peak_source": hsrc,
+            "hbm_frac": round(corpus_bytes / p50 / 1e9 / hbm, 4), "bound": bound,
+            "queries_per_s": round(b / p50, 1),
+            "launches_per_call": 5, "steps": len(ms)}
 
 
 def run_int32(rbf, steps, warmup):
@@ -288,11 +295,12 @@ def run_int32(rbf, steps, warmup):
     out = {"workload": "n=100,000,000 int32 uniform over the full range"}
     dv = torch.empty(64, dtype=torch.int32, device="cuda")
     dp = torch.empty(64, dtype=torch.int64, device="cuda")
+    hbm, _ = hbm_peak()
     for k in (20, 50):
         ms = time_device(st, lambda: e.topk_int32_dev(x, k, dv, dp), steps, warmup)
         p50 = percentile(ms, 50) * 1e-3
         out[f"k{k}"] = {"p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
-                        "gbs": round(4.0 * n / p50 / 1e9, 1)}
+                        "gbs": round(4.0 * n / p50 / 1e9, 1), "hbm_frac": round(4.0 * n / p50 / 1e9 / hbm, 4)}
     e.close()
     return out
 
