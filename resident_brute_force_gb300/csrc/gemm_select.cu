@@ -537,6 +537,332 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// ------------------------------------------------ CTA-pair variant (2 SMs)
+//
+// For 129-256 queries. A cluster of two CTAs computes each 256-row corpus tile
+// against all 256 queries with tcgen05.mma.cta_group::2 (M = 256, N = 256,
+// K = 16). Per 64-wide K chunk each CTA stages only its own 128 queries (A)
+// and 128 of the tile's rows (B), 32 KB, so six stages fit; the MMA reads
+// both CTAs' shared memory and writes each CTA's TMEM (its 128 queries x 256
+// rows). The even CTA of the pair issues the MMAs and multicasts each commit
+// to both CTAs' barriers; the odd CTA's loads complete on the even CTA's full
+// barrier, and both CTAs' epilogues release an accumulator on the even CTA's
+// barrier. Per SM and stage this moves 2/3 of the bytes of the single-CTA
+// kernel for the same tensor work.
+
+constexpr int kPairStages = 6;
+constexpr int kPairStageBytes = 2 * kSubTileBytes;  // A (own 128 queries) | B (own 128 rows)
+constexpr int kPairTileRows = 256;
+constexpr int kPairAccArrivals = 2 * kEpiWarps;     // epilogue warps of both CTAs
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the variable at `p` in the CTA of the given rank.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` in both CTAs of the pair when every MMA issued so far
+// is done.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+// Tiled TMA loads into this CTA's shared memory whose completion is counted
+// on the barrier at cluster address `bar` (the even CTA's).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+template <int KP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_select_pair_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
+                            const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);  // [kCandCap][256]
+  uint64_t* full = cand + kCandCap * 256;
+  uint64_t* empty = full + kPairStages;
+  uint64_t* acc_full = empty + kPairStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+  const int num_pair_tiles = static_cast<int>((p.n + kPairTileRows - 1) / kPairTileRows);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);   // the even CTA's producer (expect_tx for both CTAs' bytes)
+      mbar_init(&empty[s], 1);  // one multicast commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kPairAccArrivals);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  // Both CTAs' barriers are initialised before either CTA signals the other.
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // --------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_c = l2_policy_evict_first();
+      const uint64_t pol_q = l2_policy_evict_last();
+      int64_t it = 0;
+      bool aborted = false;
+      for (int t = cluster; t < num_pair_tiles && !aborted; t += nclusters) {
+        for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
+          const int s = static_cast<int>(it % kPairStages);
+          const uint32_t u = static_cast<uint32_t>(it / kPairStages);
+          if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1u, p.timeout_ns)) {
+            atomicOr(p.err, kErrProducerTimeout);
+            aborted = true;
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+            aborted = true;
+            break;
+          }
+          uint8_t* st = ring + static_cast<size_t>(s) * kPairStageBytes;
+          if (leader) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * kPairStageBytes));
+          const uint32_t bar = cluster_addr(&full[s], 0);
+          tma_load_2d_pair(st, &tmap_q, kc * kKChunk, p.q_row0 + static_cast<int>(rank) * 128, bar, pol_q);
+          tma_load_3d_pair(st + kSubTileBytes, &tmap_c, 0, 0, (2 * t + static_cast<int>(rank)) * p.kchunks + kc, bar,
+                           pol_c);
+        }
+      }
+      if (aborted) {
+        abort_flag = 1;
+        // The even CTA lets every stage it armed land before the pair can exit
+        // (those phases count both CTAs' loads).
+        if (leader) {
+          for (int64_t i = (it > kPairStages ? it - kPairStages : 0); i < it; ++i) {
+            const int s = static_cast<int>(i % kPairStages);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kPairStages) & 1u, p.timeout_ns))
+              atomicOr(p.err, kErrDrainTimeout);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      if (leader) {
+        constexpr uint32_t idesc = make_idesc(256, kPairTileRows);
+        int64_t it = 0;
+        int tile_i = 0;
+        bool aborted = false;
+        for (int t = cluster; t < num_pair_tiles && !aborted; t += nclusters, ++tile_i) {
+          const int b = tile_i & 1;
+          const uint32_t ub = static_cast<uint32_t>(tile_i >> 1);
+          if (ub > 0 && !mbar_wait(&acc_empty[b], (ub - 1) & 1u, p.timeout_ns)) {
+            atomicOr(p.err, kErrConsumerTimeout);
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
+            const int s = static_cast<int>(it % kPairStages);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kPairStages) & 1u, p.timeout_ns)) {
+              atomicOr(p.err, kErrConsumerTimeout);
+              aborted = true;
+              break;
+            }
+            tc_fence_after();
+            const uint8_t* st = ring + static_cast<size_t>(s) * kPairStageBytes;
+            const uint64_t adesc = sw128_kmajor_desc(st);
+            const uint64_t bdesc = sw128_kmajor_desc(st + kSubTileBytes);
+            const uint32_t d = tmem_base + static_cast<uint32_t>(b * kPairTileRows);
+#pragma unroll
+            for (int k = 0; k < kKChunk / 16; ++k)
+              umma_bf16_pair(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                             (kc | k) != 0);
+            umma_commit_pair(&empty[s]);  // both CTAs' stage s is free once these MMAs finish
+          }
+          if (aborted) break;
+          umma_commit_pair(&acc_full[b]);  // both CTAs' accumulators are complete
+        }
+        if (aborted) abort_flag = 1;
+        // Every MMA (they read both CTAs' shared memory and write both TMEMs)
+        // must be finished before either CTA releases TMEM or exits.
+        umma_commit_pair(drain);
+      }
+      if (!mbar_wait(drain, 0, p.timeout_ns)) atomicOr(p.err, kErrDrainTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int e = warp - 2;
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int h = e >> 2;             // which 128 of the tile's 256 rows
+    const int qlocal = quad * 32 + lane;
+    const int qidx = static_cast<int>(rank) * 128 + qlocal;  // query within this launch
+    const int slot = h * 128 + qlocal;                        // candidate buffer column
+    const uint32_t acc_empty_leader0 = cluster_addr(&acc_empty[0], 0);
+    const uint32_t acc_empty_leader1 = cluster_addr(&acc_empty[1], 0);
+    uint64_t L[KP];
+#pragma unroll
+    for (int i = 0; i < KP; ++i) L[i] = 0;
+    uint64_t floor_key = 0;
+    if (p.theta0 && qidx < p.q_count) {
+      const uint64_t b0 = p.theta0[p.q_out0 + qidx];
+      floor_key = b0 > 0 ? b0 - 1 : 0;
+    }
+    uint64_t theta = floor_key;
+    float theta_f = floor_key ? key_score(floor_key + 1) : 0.0f;
+    bool filling = floor_key == 0;
+    int cnt = 0;
+
+    auto merge_buffer = [&]() {
+      const int batches = static_cast<int>((__reduce_max_sync(kFullMask, static_cast<unsigned>(cnt)) + 7u) >> 3);
+#pragma unroll 1
+      for (int b8 = 0; b8 < batches * 8; b8 += 8) {
+        uint64_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = (b8 + i < cnt) ? cand[(b8 + i) * 256 + slot] : 0ull;
+        sort8_desc(c);
+        list_merge8<KP>(L, c);
+      }
+      cnt = 0;
+      theta = umax64(list_get<KP>(L, p.k - 1), floor_key);
+      filling = theta == 0;
+      theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
+    };
+
+    int tile_i = 0;
+    for (int t = cluster; t < num_pair_tiles; t += nclusters, ++tile_i) {
+      const int b = tile_i & 1;
+      if (!__all_sync(kFullMask, mbar_wait(&acc_full[b], static_cast<uint32_t>(tile_i >> 1) & 1u, p.timeout_ns))) {
+        if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
+        abort_flag = 1;
+        break;
+      }
+      if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) break;
+      tc_fence_after();
+      const int64_t row0 = static_cast<int64_t>(t) * kPairTileRows + h * 128;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(b * kPairTileRows + h * 128);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float s64[64];
+        tmem_ld64(tbase + static_cast<uint32_t>(hh * 64), s64);
+        if (hh == 1) {
+          // The accumulator may be overwritten from here on: release it on
+          // the even CTA's barrier.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(b ? acc_empty_leader1 : acc_empty_leader0);
+        }
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const float(&sc)[32] = *reinterpret_cast<const float(*)[32]>(&s64[c2 * 32]);
+          const int64_t rb = row0 + hh * 64 + c2 * 32;
+          uint32_t m = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
+          if (filling) m = 0xFFFFFFFFu;
+          if (p.n - rb < 32) m &= (p.n - rb > 0) ? ((1u << (p.n - rb)) - 1u) : 0u;
+          uint32_t u = __reduce_or_sync(kFullMask, m);
+          while (u) {
+            const int j = __ffs(u) - 1;
+            u &= u - 1;
+            if (m & (1u << j)) {
+              const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j));
+              if (key > theta) {
+                cand[cnt * 256 + slot] = key;
+                ++cnt;
+              }
+            }
+            if (__any_sync(kFullMask, cnt == kCandCap)) merge_buffer();
+          }
+        }
+      }
+    }
+    if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
+    if (qidx < p.q_count) {
+      uint64_t* dst =
+          p.partials + (static_cast<size_t>(p.q_out0 + qidx) * gridDim.x + static_cast<size_t>(cluster * 2 + h)) * 32;
+#pragma unroll
+      for (int i = 0; i < KP; ++i) dst[i] = L[i];
+#pragma unroll
+      for (int i = KP; i < 32; ++i) dst[i] = 0ull;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // Neither CTA releases TMEM or exits while the other may still signal it.
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
 // --------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -564,6 +890,35 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params&
   }
   fn<<<grid, kThreads, smem, st>>>(tq, tc, p);
   return cudaGetLastError();
+}
+
+int pair_smem_bytes() {
+  return 1024 + kPairStages * kPairStageBytes + kCandCap * 256 * 8 + (2 * kPairStages + 5) * 8 + 16;
+}
+
+template <int KP>
+cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
+  auto fn = gemm_select_pair_kernel<KP>;
+  const int smem = pair_smem_bytes();
+  static int configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, tq, tc, p);
 }
 
 // fp32 [rows][src_pitch] -> bf16 [rows][dst_pitch], zero past `cols` and for
@@ -680,6 +1035,14 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   }
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
+  if (a.grid < 2 || a.grid % 2 != 0) return cudaErrorInvalidValue;
+  if (a.q_count > 128) {
+    // Two M tiles: a CTA pair per 256-row tile (lists per query = grid).
+    if (a.k <= 8) return launch_pair_t<8>(tq, tc, p, a.grid, stream);
+    if (a.k <= 16) return launch_pair_t<16>(tq, tc, p, a.grid, stream);
+    if (a.k <= 32) return launch_pair_t<32>(tq, tc, p, a.grid, stream);
+    return cudaErrorInvalidValue;
+  }
   if (a.k <= 8) return launch_t<8>(tq, tc, p, a.grid, stream);
   if (a.k <= 16) return launch_t<16>(tq, tc, p, a.grid, stream);
   if (a.k <= 32) return launch_t<32>(tq, tc, p, a.grid, stream);

@@ -102,7 +102,7 @@ struct GemmSelectLaunch {
   int q_count;               // queries in this launch, 1..256
   int q_out0;                // first query of this launch in the partials layout
   int k;
-  int grid;
+  int grid;                  // even: 2 x min(ceil(n / 256), SMs / 2); also the lists per query
   uint64_t timeout_ns;
   const uint64_t* theta0;    // optional per-query lower bound on the K-th key (keys >= it are kept)
   int bound_mode = 0;        // 1: no selection; each CTA writes, per query, the best key of every
