@@ -68,15 +68,16 @@ __device__ __forceinline__ void emit(const Params& p, int e, uint64_t key) {
 }
 
 // Copy the first k keys of lists [l0, l0 + count) to dst (list-major, k per
-// list) with eight loads in flight per thread before any is stored, so the
-// copy costs one L2 round trip per 8 x threads keys.
-template <int KP, int NT>
+// list) with U loads in flight per thread before any is stored, so the copy
+// costs one L2 round trip per U x threads keys (16 for CTAs of up to 256
+// threads, 8 for wider ones, which must stay within 64 registers).
+template <int KP, int NT, int U = (NT <= 256 ? 16 : 8)>
 __device__ __forceinline__ void stage_heads(uint64_t* dst, const uint64_t* base, int l0, int count, int k) {
   const int total = count * k;
-  for (int i0 = 0; i0 < total; i0 += 8 * NT) {
-    uint64_t r[8];
+  for (int i0 = 0; i0 < total; i0 += U * NT) {
+    uint64_t r[U];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int i = i0 + u * NT + static_cast<int>(threadIdx.x);
       r[u] = 0;
       if (i < total) {
@@ -85,7 +86,7 @@ __device__ __forceinline__ void stage_heads(uint64_t* dst, const uint64_t* base,
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int i = i0 + u * NT + static_cast<int>(threadIdx.x);
       if (i < total) dst[i] = r[u];
     }
