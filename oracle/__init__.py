@@ -58,14 +58,16 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     P = ctypes.c_void_p
     i64, i32 = ctypes.c_int64, ctypes.c_int32
     lib.oracle_scores.argtypes = [P, i64, i32, P, P]
+    lib.oracle_scores_cosine.argtypes = [P, i64, i32, P, P]
     lib.oracle_topk.argtypes = [P, i64, i32, P, i32, P, P]
+    lib.oracle_topk_cosine.argtypes = [P, i64, i32, P, i32, P, P]
     lib.oracle_topk_batch.argtypes = [P, i64, i32, P, i32, i32, P, P]
     lib.oracle_topk_int32.argtypes = [P, i64, i32, P, P]
     lib.oracle_round_bf16.argtypes = [P, P, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
-    for f in ("oracle_scores", "oracle_topk", "oracle_topk_batch", "oracle_topk_int32",
-              "oracle_round_bf16"):
+    for f in ("oracle_scores", "oracle_scores_cosine", "oracle_topk", "oracle_topk_cosine", "oracle_topk_batch",
+              "oracle_topk_int32", "oracle_round_bf16"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -103,6 +105,27 @@ class Oracle:
         sc = np.empty(k, dtype=np.float64)
         if self.lib.oracle_topk(_ptr(c), n, d, _ptr(q), k, _ptr(idx), _ptr(sc)):
             raise ValueError("oracle_topk rejected its arguments")
+        return idx, sc
+
+    def scores_cosine(self, corpus, query) -> np.ndarray:
+        """All N double cosine scores of one query (``oracle_scores_cosine``)."""
+        c, q = _f32(corpus), _f32(query).reshape(-1)
+        n, d = c.shape
+        if q.shape[0] != d:
+            raise ValueError("query length != D")
+        out = np.empty(n, dtype=np.float64)
+        if self.lib.oracle_scores_cosine(_ptr(c), n, d, _ptr(q), _ptr(out)):
+            raise ValueError("oracle_scores_cosine rejected its arguments")
+        return out
+
+    def topk_cosine(self, corpus, query, k: int):
+        """(indices int64[K], cosine scores float64[K]) best-first (``oracle_topk_cosine``)."""
+        c, q = _f32(corpus), _f32(query).reshape(-1)
+        n, d = c.shape
+        idx = np.empty(k, dtype=np.int64)
+        sc = np.empty(k, dtype=np.float64)
+        if self.lib.oracle_topk_cosine(_ptr(c), n, d, _ptr(q), k, _ptr(idx), _ptr(sc)):
+            raise ValueError("oracle_topk_cosine rejected its arguments")
         return idx, sc
 
     def topk_batch(self, corpus, queries, k: int):
@@ -159,6 +182,14 @@ def topk(corpus, query, k):
 
 def topk_batch(corpus, queries, k):
     return get().topk_batch(corpus, queries, k)
+
+
+def scores_cosine(corpus, query):
+    return get().scores_cosine(corpus, query)
+
+
+def topk_cosine(corpus, query, k):
+    return get().topk_cosine(corpus, query, k)
 
 
 def topk_int32(x, k):

@@ -17,6 +17,11 @@
  *   a higher score is better; on an exact score tie the lower row index is
  *   better.
  *
+ *   Cosine similarity (same article, section 4 step 2, the scoring kernel's
+ *   cosine mode, and the later section on the two flavours of similarity):
+ *   the inner product divided by the product of the query's and the row's L2
+ *   norms; a row whose denominator is not positive scores -infinity.
+ *
  *   The flat int32 formulation (CUDA programming model series 9, sections 1
  *   and 2.1): the K largest values of an int32 array. Positions are returned
  *   too and the lower position wins ties (that page tracks no positions; the
@@ -24,7 +29,9 @@
  *
  * Readings taken where the pages are silent:
  *   - Scores are accumulated in double, in index order d = 0..D-1. Each
- *     fp32 x fp32 product is exact in double.
+ *     fp32 x fp32 product is exact in double. Cosine norms are the square
+ *     roots of double sums of squares in the same order, and the quotient is
+ *     taken in double.
  *   - A NaN score ranks as -infinity (the tie rule is not a strict order with
  *     NaN). -0.0 and +0.0 compare equal, so they tie and the index decides.
  *   - The selection is a full sort of all (score, index) pairs by the rule,
@@ -104,19 +111,35 @@ int oracle_scores(const float* corpus, int64_t n, int32_t d, const float* query,
   return 0;
 }
 
-/* Top-K of one query: score every row, sort all N pairs best-first, keep K.
- * out_idx gets K row indices, out_score their double scores. */
-int oracle_topk(const float* corpus, int64_t n, int32_t d, const float* query, int32_t k,
-                int64_t* out_idx, double* out_score) {
-  if (!corpus || !query || !out_idx || !out_score || n < 1 || d < 1 || k < 1 || k > n) return 1;
-  double* sigma = (double*)malloc(sizeof(double) * (size_t)n);
-  oracle_pair* pairs = (oracle_pair*)malloc(sizeof(oracle_pair) * (size_t)n);
-  if (!sigma || !pairs) {
-    free(sigma);
-    free(pairs);
-    return 2;
+/* cos_i = (sum_d c[i, d] * q[d]) / (||c_i|| * ||q||) in double, for every
+ * row i, with ||x|| = sqrt(sum_d x[d]^2). A denominator that is not positive
+ * (a zero row or a zero query) gives -infinity, as does a NaN quotient. */
+int oracle_scores_cosine(const float* corpus, int64_t n, int32_t d, const float* query, double* out) {
+  if (!corpus || !query || !out || n < 0 || d < 1) return 1;
+  double qq = 0.0;
+  for (int32_t j = 0; j < d; ++j) qq += (double)query[j] * (double)query[j];
+  const double qnorm = sqrt(qq);
+  int64_t i;
+#pragma omp parallel for schedule(static)
+  for (i = 0; i < n; ++i) {
+    const float* row = corpus + i * (int64_t)d;
+    double dot = 0.0, cc = 0.0;
+    for (int32_t j = 0; j < d; ++j) {
+      dot += (double)row[j] * (double)query[j];
+      cc += (double)row[j] * (double)row[j];
+    }
+    const double denom = qnorm * sqrt(cc);
+    double cosv = denom > 0.0 ? dot / denom : -INFINITY;
+    if (isnan(cosv)) cosv = -INFINITY;
+    out[i] = cosv;
   }
-  oracle_scores(corpus, n, d, query, sigma);
+  return 0;
+}
+
+/* Sort all N (score, index) pairs best-first under the rule and keep K. */
+static int select_topk(const double* sigma, int64_t n, int32_t k, int64_t* out_idx, double* out_score) {
+  oracle_pair* pairs = (oracle_pair*)malloc(sizeof(oracle_pair) * (size_t)n);
+  if (!pairs) return 2;
   for (int64_t i = 0; i < n; ++i) {
     pairs[i].score = sigma[i];
     pairs[i].index = i;
@@ -126,9 +149,35 @@ int oracle_topk(const float* corpus, int64_t n, int32_t d, const float* query, i
     out_idx[j] = pairs[j].index;
     out_score[j] = pairs[j].score;
   }
-  free(sigma);
   free(pairs);
   return 0;
+}
+
+/* Top-K of one query: score every row, sort all N pairs best-first, keep K.
+ * out_idx gets K row indices, out_score their double scores. cosine != 0
+ * scores by cosine similarity instead of the inner product. */
+static int topk_metric(const float* corpus, int64_t n, int32_t d, const float* query, int32_t k, int cosine,
+                       int64_t* out_idx, double* out_score) {
+  if (!corpus || !query || !out_idx || !out_score || n < 1 || d < 1 || k < 1 || k > n) return 1;
+  double* sigma = (double*)malloc(sizeof(double) * (size_t)n);
+  if (!sigma) return 2;
+  if (cosine)
+    oracle_scores_cosine(corpus, n, d, query, sigma);
+  else
+    oracle_scores(corpus, n, d, query, sigma);
+  const int rc = select_topk(sigma, n, k, out_idx, out_score);
+  free(sigma);
+  return rc;
+}
+
+int oracle_topk(const float* corpus, int64_t n, int32_t d, const float* query, int32_t k,
+                int64_t* out_idx, double* out_score) {
+  return topk_metric(corpus, n, d, query, k, 0, out_idx, out_score);
+}
+
+int oracle_topk_cosine(const float* corpus, int64_t n, int32_t d, const float* query, int32_t k,
+                       int64_t* out_idx, double* out_score) {
+  return topk_metric(corpus, n, d, query, k, 1, out_idx, out_score);
 }
 
 /* B queries (row-major B x D), one top-K each: out arrays are B x K. */

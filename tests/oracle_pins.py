@@ -314,10 +314,116 @@ def pin_bf16_rounding(o) -> None:
     assert np.array_equal(o.round_bf16(x), ref)
 
 
+# --------------------------------------------------------------- cosine pins
+#
+# Cosine similarity (GPU-Resident Top-K for Agentic RAG, section 4 step 2,
+# cosine mode): inner product / (||q|| * ||c_i||), -inf when that denominator
+# is not positive.
+
+# Integer vectors with integer L2 norms: the cosine of any two is the exact
+# rational dot / (|a| |b|).
+_PYTH = [((3, 4, 0), 5), ((0, 3, 4), 5), ((2, 3, 6), 7), ((1, 4, 8), 9), ((4, 4, 7), 9),
+         ((2, 6, 9), 11), ((6, 2, 3), 7), ((-2, 3, -6), 7), ((8, -4, 1), 9), ((0, 0, 5), 5)]
+
+
+def pin_cosine_exact_rationals(o) -> None:
+    """Integer rows and queries with integer norms: every cosine equals the
+    rational dot / (|c| |q|) to within one rounding of each double step."""
+    c = np.array([v for v, _ in _PYTH], dtype=np.float32)
+    norms = [nv for _, nv in _PYTH]
+    for qi, (qv, qn) in enumerate(_PYTH):
+        q = np.array(qv, dtype=np.float32)
+        got = o.scores_cosine(c, q)
+        for i, (cv, cn) in enumerate(_PYTH):
+            exact = Fraction(sum(a * b for a, b in zip(cv, qv)), cn * qn)
+            assert abs(Fraction(float(got[i])) - exact) <= Fraction(4, 2 ** 53), (qi, i, got[i], exact)
+
+
+def pin_cosine_parallel_and_orthogonal(o) -> None:
+    """Rows alpha * q give +1 (alpha > 0) or -1 (alpha < 0), to rounding;
+    with alpha a power of two they are bit-identical, so they tie and come
+    first by index; rows orthogonal to q give exactly 0."""
+    rng = np.random.default_rng(151)
+    d = 24
+    q = rng.standard_normal(d).astype(np.float32)
+    q[5] = 0.0
+    alphas = [4.0, 0.5, -2.0, 0.125, -7.5, 2.0, 3.0, 11.0]
+    rows = [(a * q.astype(np.float64)).astype(np.float32) for a in alphas]
+    e5 = np.zeros(d, dtype=np.float32)
+    e5[5] = 4.0
+    rows += [e5]
+    c = np.stack(rows)
+    got = o.scores_cosine(c, q)
+    for a, g in zip(alphas, got[:8]):
+        assert abs(g - np.sign(a)) < 1e-6, (a, g)
+    assert got[0] == got[1] == got[3] == got[5]
+    assert got[8] == 0.0
+    idx, _ = o.topk_cosine(c[[0, 1, 2, 3, 4, 5, 8]], q, 4)
+    assert list(idx) == [0, 1, 3, 5], list(idx)
+
+
+def pin_cosine_zero_vectors(o) -> None:
+    """A zero row scores -inf; a zero query scores every row -inf, so the
+    top-K is rows 0..K-1 (ties by index)."""
+    rng = np.random.default_rng(161)
+    c = rng.standard_normal((30, 8)).astype(np.float32)
+    c[4] = 0.0
+    q = rng.standard_normal(8).astype(np.float32)
+    got = o.scores_cosine(c, q)
+    assert got[4] == -np.inf and np.all(np.isfinite(np.delete(got, 4)))
+    idx, _ = o.topk_cosine(c, q, 30)
+    assert idx[-1] == 4
+    z = np.zeros(8, dtype=np.float32)
+    assert np.all(o.scores_cosine(c, z) == -np.inf)
+    idx, sc = o.topk_cosine(c, z, 6)
+    assert list(idx) == list(range(6)) and np.all(sc == -np.inf)
+
+
+def pin_cosine_scale_invariance(o) -> None:
+    """Scaling a row or the query by a positive power of two changes no
+    cosine (bit for bit: every double step scales exactly); any positive
+    scale changes it by rounding only. Rows scaled by powers of two tie with
+    their originals, and the lower index comes first."""
+    rng = np.random.default_rng(171)
+    n, d = 40, 33
+    c = rng.standard_normal((n, d)).astype(np.float32)
+    q = rng.standard_normal(d).astype(np.float32)
+    base = o.scores_cosine(c, q)
+    p2 = (2.0 ** rng.integers(-6, 7, size=n)).astype(np.float32)
+    assert np.array_equal(o.scores_cosine(c * p2[:, None], q * np.float32(8.0)), base)
+    s = rng.uniform(0.1, 10.0, size=n).astype(np.float64)
+    cs = (c.astype(np.float64) * s[:, None]).astype(np.float32)
+    np.testing.assert_allclose(o.scores_cosine(cs, q * np.float32(0.3)), base, rtol=1e-6, atol=1e-7)
+    dup = np.concatenate([c, c[7:8] * np.float32(4.0), c[7:8] * np.float32(0.25)])
+    idx, sc = o.topk_cosine(dup, c[7], 3)
+    assert list(idx) == [7, n, n + 1] and sc[0] == sc[1] == sc[2]
+
+
+def pin_cosine_unit_rows_match_ip_and_order(o) -> None:
+    """On rows and a query normalised to unit length (in double, then fp32)
+    the cosine equals the inner product to fp32 rounding of the norms; and
+    K = N lists rows in numpy's stable descending order of the scores."""
+    rng = np.random.default_rng(181)
+    n, d = 300, 64
+    c64 = rng.standard_normal((n, d))
+    c = (c64 / np.linalg.norm(c64, axis=1, keepdims=True)).astype(np.float32)
+    q64 = rng.standard_normal(d)
+    q = (q64 / np.linalg.norm(q64)).astype(np.float32)
+    np.testing.assert_allclose(o.scores_cosine(c, q), o.scores(c, q), rtol=0, atol=1e-6)
+    c2 = rng.standard_normal((n, d)).astype(np.float32)
+    c2[17] = c2[3]
+    sig = o.scores_cosine(c2, q)
+    idx, sc = o.topk_cosine(c2, q, n)
+    assert np.array_equal(idx, np.argsort(-sig, kind="stable"))
+    assert np.array_equal(sc, sig[idx])
+
+
 ALL_PINS = [
     pin_subsets, pin_full_order_stable_sort, pin_d1_closed_form, pin_scaled_query_rows,
     pin_basis_rows, pin_duplicates_and_all_equal, pin_dyadic_exact, pin_planted,
     pin_error_bound, pin_invariants, pin_nan_and_signed_zero, pin_batch_matches_rows,
     pin_i32_closed_forms, pin_i32_extremes, pin_i32_lexsort, pin_i32_subsets,
     pin_bf16_rounding,
+    pin_cosine_exact_rationals, pin_cosine_parallel_and_orthogonal, pin_cosine_zero_vectors,
+    pin_cosine_scale_invariance, pin_cosine_unit_rows_match_ip_and_order,
 ]

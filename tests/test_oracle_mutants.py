@@ -33,6 +33,14 @@ MUTANTS = [
     ("i32_position_shift", "pairs[i].position = i;", "pairs[i].position = i + 1;"),
     ("bf16_truncate", "bits += 0x7FFFu + lsb;", "(void)lsb;"),
     ("bf16_ties_up", "bits += 0x7FFFu + lsb;", "bits += 0x8000u;"),
+    ("cos_no_query_norm", "const double denom = qnorm * sqrt(cc);", "const double denom = sqrt(cc);"),
+    ("cos_squared_row_norm", "const double denom = qnorm * sqrt(cc);", "const double denom = qnorm * cc;"),
+    ("cos_zero_denominator_scores_zero", "double cosv = denom > 0.0 ? dot / denom : -INFINITY;",
+     "double cosv = denom > 0.0 ? dot / denom : 0.0;"),
+    ("cos_row_norm_from_query", "cc += (double)row[j] * (double)row[j];",
+     "cc += (double)query[j] * (double)query[j];"),
+    ("cos_topk_scores_inner_product", "  if (cosine)\n", "  if (0)\n"),
+    ("cos_query_norm_drops_last", "for (int32_t j = 0; j < d; ++j) qq +=", "for (int32_t j = 0; j < d - 1; ++j) qq +="),
 ]
 
 
