@@ -60,6 +60,15 @@ typedef enum rbf_status {
 /* rbf_create flags. 0 means RBF_FLAG_FP32_CORPUS. */
 #define RBF_FLAG_FP32_CORPUS 0x1u /* keep the fp32 corpus: single-query path */
 #define RBF_FLAG_BF16_CORPUS 0x2u /* also keep a bf16 copy: batched path */
+/* Score by cosine similarity instead of the inner product: the inner product
+ * divided by the product of the query's and the row's L2 norms, and -infinity
+ * for a row whose denominator is not positive (GPU-Resident Top-K for Agentic
+ * RAG, section 4 step 2, the scoring kernel's cosine mode). Rows are divided
+ * by their norms once at upload (the stored corpus is the normalised one) and
+ * every query at every call, as the same article suggests; a zero-norm row or
+ * query scores -infinity everywhere. Applies to every float search entry
+ * point of the engine; topk_int32 is unaffected. */
+#define RBF_FLAG_COSINE 0x4u
 
 /* Engine options for rbf_set_option (launch shape of the scoring kernel). */
 typedef enum rbf_option {

@@ -26,6 +26,7 @@ RBF_MAX_K = 256
 RBF_MAX_D = 8192
 RBF_FLAG_FP32_CORPUS = 0x1
 RBF_FLAG_BF16_CORPUS = 0x2
+RBF_FLAG_COSINE = 0x4
 
 RBF_OPT_CTAS_PER_SM = 1
 RBF_OPT_STAGE_BYTES = 2

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "librbf.so")
 
-SOURCES = ["engine.cu", "score_select.cu", "merge.cu", "topk_i32.cu", "noalloc.cu", "gemm_select.cu"]
+SOURCES = ["engine.cu", "score_select.cu", "merge.cu", "topk_i32.cu", "noalloc.cu", "gemm_select.cu", "normalize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

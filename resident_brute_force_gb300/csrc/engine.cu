@@ -68,6 +68,7 @@ struct rbf_engine {
 
   // Workspaces (device).
   float* query = nullptr;        // max_batch * max_pitch floats
+  float* qnorm = nullptr;        // cosine mode: the unit-length query, max_pitch floats
   uint64_t* partials = nullptr;  // partials_cap keys
   uint64_t* i32_theta0 = nullptr;  // int32 path: K-th key of the element sample
   size_t partials_cap = 0;
@@ -169,6 +170,12 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k) {
   ScoreShape sh;
   if (!score_shape(e, k, &sh)) return RBF_ERR_UNSUPPORTED;
   if (static_cast<size_t>(sh.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+  if (e->flags & RBF_FLAG_COSINE) {
+    // Rows are unit length already; scoring the unit-length query gives the
+    // cosine directly.
+    RBF_LAUNCH(e, launch_normalize_query(d_query, e->d, e->pitch, e->qnorm, e->stream));
+    d_query = e->qnorm;
+  }
   ScoreSelectLaunch a;
   a.corpus = e->corpus;
   a.query = d_query;
@@ -243,6 +250,7 @@ void release(rbf_engine* e) {
   cudaFree(e->errw);
   cudaFree(e->counters);
   cudaFree(e->i32_theta0);
+  cudaFree(e->qnorm);
   cudaFree(e->result);
   cudaFreeHost(e->h_query);
   cudaFreeHost(e->h_result);
@@ -273,8 +281,8 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   if (max_n < 1 || max_n > INT32_MAX || max_d < 1 || max_d > RBF_MAX_D || max_k < 1 || max_k > RBF_MAX_K ||
       max_batch < 1 || max_batch > kMaxBatch)
     return RBF_ERR_INVALID_VALUE;
-  if (flags & ~(RBF_FLAG_FP32_CORPUS | RBF_FLAG_BF16_CORPUS)) return RBF_ERR_INVALID_VALUE;
-  if (flags == 0) flags = RBF_FLAG_FP32_CORPUS;
+  if (flags & ~(RBF_FLAG_FP32_CORPUS | RBF_FLAG_BF16_CORPUS | RBF_FLAG_COSINE)) return RBF_ERR_INVALID_VALUE;
+  if (!(flags & (RBF_FLAG_FP32_CORPUS | RBF_FLAG_BF16_CORPUS))) flags |= RBF_FLAG_FP32_CORPUS;
 
   rbf_engine* e = new (std::nothrow) rbf_engine();
   if (!e) return RBF_ERR_OUT_OF_MEMORY;
@@ -327,6 +335,8 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
     ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
   }
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  if (flags & RBF_FLAG_COSINE)
+    ok = ok && cudaMalloc(&e->qnorm, static_cast<size_t>(e->max_pitch) * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->counters, 8 * sizeof(unsigned)) == cudaSuccess;
@@ -418,6 +428,8 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
     RBF_COPY(e, cudaMemset2DAsync(e->corpus + d, static_cast<size_t>(pitch) * 4, 0,
                                   static_cast<size_t>(pitch - d) * 4, static_cast<size_t>(n), e->stream));
   }
+  if (e->flags & RBF_FLAG_COSINE)
+    RBF_LAUNCH(e, launch_normalize_rows(e->corpus, n, d, pitch, e->num_sms, e->stream));
   if (e->corpus_bf16) {
     const int pb = static_cast<int>(align_up(static_cast<size_t>(d), kBf16PitchAlign));
     RBF_LAUNCH(e, launch_to_bf16_tiled(e->corpus, pitch, e->corpus_bf16, n, pb, d, e->num_sms, e->stream));
@@ -488,8 +500,13 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   if (k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
   if (!e->tmaps_ready) return RBF_ERR_NOT_READY;
   const int64_t rows_total = static_cast<int64_t>(align_up(static_cast<size_t>(b), 128));
-  RBF_LAUNCH(e, launch_to_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d, e->num_sms,
-                               e->stream));
+  if (e->flags & RBF_FLAG_COSINE) {
+    RBF_LAUNCH(e, launch_normalize_queries_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d,
+                                                e->num_sms, e->stream));
+  } else {
+    RBF_LAUNCH(e, launch_to_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d, e->num_sms,
+                                 e->stream));
+  }
   // The scoring + select kernel over rows [0, rows): one launch per group of
   // up to 256 queries; returns the number of per-CTA lists per query.
   auto score_groups = [&](int64_t rows, int bound_mode, const uint64_t* theta0, int* lists) -> rbf_status {
