@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-gate", action="store_true")
     ap.add_argument("--no-batched", action="store_true")
     ap.add_argument("--no-int32", action="store_true")
+    ap.add_argument("--no-cosine", action="store_true")
     ap.add_argument("--schedule", type=int, default=None)
     ap.add_argument("--ctas-per-sm", type=int, default=None)
     ap.add_argument("--stage-bytes", type=int, default=None)
@@ -284,6 +285,33 @@ def run_batched(rbf, steps, warmup):
             "launches_per_call": 5, "steps": len(ms)}
 
 
+def run_cosine(rbf, c, qs, planted, steps, warmup):
+    """Cosine mode on the headline workload (N=1M, D=1024, K=8): rows made
+    unit length at upload; each step is the scoring kernel (which scales the
+    query to unit length first) + the merge, through search_resident_dev."""
+    import torch
+    n, d = c.shape
+    st = torch.cuda.Stream()
+    e = rbf.Engine(n, d, 8, stream=st, flags=rbf.RBF_FLAG_COSINE)
+    e.upload_corpus_rowmajor(c)
+    for j in range(0, len(qs), max(1, len(qs) // 10)):
+        idx, _ = e.search_resident(qs[j], 8)
+        assert set(idx.tolist()) <= set(planted[j].tolist()), f"cosine: planted rows missing for query {j}"
+    dq = torch.from_numpy(qs).cuda()
+    di = torch.empty(8, dtype=torch.int32, device="cuda")
+    ds = torch.empty(8, dtype=torch.float32, device="cuda")
+    nq = len(qs)
+    it = iter(range(10 ** 9))
+    ms = time_device(st, lambda: e.search_resident_dev(dq[next(it) % nq], 8, di, ds), steps, warmup)
+    e.close()
+    p50 = percentile(ms, 50) * 1e-3
+    hbm, _ = hbm_peak()
+    gbs = n * d * 4 / p50 / 1e9
+    return {"workload": "cosine mode, N=1,000,000 x D=1024 fp32 (rows unit length at upload), K=8",
+            "p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
+            "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "launches_per_step": 2, "steps": len(ms)}
+
+
 def run_int32(rbf, steps, warmup):
     """Flat int32 two-stage top-K: 100,000,000 values, K=20 and K=50."""
     import torch
@@ -450,6 +478,7 @@ def main():
                 "vs_8tbs": round(achieved / 8000.0, 4)}
 
     eng.close()
+    cosine = run_cosine(rbf, c, qs, planted, 200, 5) if (rank == 0 and not args.no_cosine) else None
     batched = run_batched(rbf, 30, 3) if (rank == 0 and not args.no_batched) else None
     int32 = run_int32(rbf, 50, 5) if (rank == 0 and not args.no_int32) else None
 
@@ -472,6 +501,8 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * args.steps, "clocks": clocks,
         }
+        if cosine is not None:
+            line["cosine"] = cosine
         if batched is not None:
             line["batched"] = batched
         if int32 is not None:

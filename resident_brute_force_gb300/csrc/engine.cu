@@ -68,7 +68,6 @@ struct rbf_engine {
 
   // Workspaces (device).
   float* query = nullptr;        // max_batch * max_pitch floats
-  float* qnorm = nullptr;        // cosine mode: the unit-length query, max_pitch floats
   uint64_t* partials = nullptr;  // partials_cap keys
   uint64_t* i32_theta0 = nullptr;  // int32 path: K-th key of the element sample
   size_t partials_cap = 0;
@@ -170,12 +169,6 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k) {
   ScoreShape sh;
   if (!score_shape(e, k, &sh)) return RBF_ERR_UNSUPPORTED;
   if (static_cast<size_t>(sh.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
-  if (e->flags & RBF_FLAG_COSINE) {
-    // Rows are unit length already; scoring the unit-length query gives the
-    // cosine directly.
-    RBF_LAUNCH(e, launch_normalize_query(d_query, e->d, e->pitch, e->qnorm, e->stream));
-    d_query = e->qnorm;
-  }
   ScoreSelectLaunch a;
   a.corpus = e->corpus;
   a.query = d_query;
@@ -192,6 +185,9 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k) {
   a.grid = sh.grid;
   a.dynamic = e->dynamic;
   a.timeout_ns = e->timeout_ns;
+  // Cosine mode: rows are unit length already; the kernel scales its copy of
+  // the query to unit length, so the inner product is the cosine.
+  a.normalize_query = (e->flags & RBF_FLAG_COSINE) ? 1 : 0;
   RBF_LAUNCH(e, launch_score_select(a, e->stream));
   e->last_lists = sh.grid;
   e->last_k = k;
@@ -250,7 +246,6 @@ void release(rbf_engine* e) {
   cudaFree(e->errw);
   cudaFree(e->counters);
   cudaFree(e->i32_theta0);
-  cudaFree(e->qnorm);
   cudaFree(e->result);
   cudaFreeHost(e->h_query);
   cudaFreeHost(e->h_result);
@@ -335,8 +330,6 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
     ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
   }
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
-  if (flags & RBF_FLAG_COSINE)
-    ok = ok && cudaMalloc(&e->qnorm, static_cast<size_t>(e->max_pitch) * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->counters, 8 * sizeof(unsigned)) == cudaSuccess;

@@ -5,9 +5,9 @@
 // positive scores -infinity (GPU-Resident Top-K for Agentic RAG, section 4
 // step 2, the scoring kernel's cosine mode). The same article notes that
 // dividing every row by its norm once at ingest turns cosine into a plain
-// inner product. That is done here: rows are scaled to unit length at upload
-// and the query at every call, so the scoring kernels are the inner-product
-// kernels unchanged. Norms are square roots of double sums of squares and
+// inner product. That is done here for the rows (at upload) and for the
+// batched queries (at every call); the single-query scoring kernel scales its
+// own copy of the query the same way. Norms are square roots of double sums of squares and
 // every element is scaled in double, then rounded to fp32 once. A vector with
 // zero norm (or a NaN or infinite element) becomes all NaN; its scores are
 // NaN, which the selection keys rank as -infinity, as the rule asks.
@@ -34,11 +34,6 @@ __device__ __forceinline__ double warp_sumsq(const float* x, int d, int lane) {
   return ss;
 }
 
-// 1 / ||x||, or NaN when the norm is zero or not finite.
-__device__ __forceinline__ double inv_norm(double ss) {
-  return (ss > 0.0 && ss <= 1.7976931348623157e308) ? 1.0 / sqrt(ss) : __longlong_as_double(0x7FF8000000000000ll);
-}
-
 // One warp per row, in place: row[j] <- row[j] / ||row|| for j < d (the
 // zero padding up to the pitch stays zero).
 __global__ void normalize_rows_kernel(float* corpus, int64_t n, int d, int pitch) {
@@ -46,16 +41,9 @@ __global__ void normalize_rows_kernel(float* corpus, int64_t n, int d, int pitch
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
     float* row = corpus + r * pitch;
-    const double inv = inv_norm(warp_sumsq(row, d, lane));
+    const double inv = inv_l2_norm(warp_sumsq(row, d, lane));
     for (int j = lane; j < d; j += 32) row[j] = static_cast<float>(static_cast<double>(row[j]) * inv);
   }
-}
-
-// One warp: out[j] = q[j] / ||q|| for j < d, 0 for d <= j < pitch.
-__global__ void normalize_query_kernel(const float* q, int d, int pitch, float* out) {
-  const int lane = threadIdx.x & 31;
-  const double inv = inv_norm(warp_sumsq(q, d, lane));
-  for (int j = lane; j < pitch; j += 32) out[j] = j < d ? static_cast<float>(static_cast<double>(q[j]) * inv) : 0.0f;
 }
 
 // One warp per query row: unit length, then bf16 (round to nearest even) into
@@ -70,7 +58,7 @@ __global__ void normalize_queries_bf16_kernel(const float* __restrict__ src, int
     __nv_bfloat16* o = dst + r * dst_pitch;
     if (r < rows) {
       const float* x = src + r * src_pitch;
-      const double inv = inv_norm(warp_sumsq(x, cols, lane));
+      const double inv = inv_l2_norm(warp_sumsq(x, cols, lane));
       for (int64_t j = lane; j < dst_pitch; j += 32)
         o[j] = __float2bfloat16_rn(j < cols ? static_cast<float>(static_cast<double>(x[j]) * inv) : 0.0f);
     } else {
@@ -84,11 +72,6 @@ __global__ void normalize_queries_bf16_kernel(const float* __restrict__ src, int
 cudaError_t launch_normalize_rows(float* corpus, int64_t n, int d, int pitch, int num_sms, cudaStream_t st) {
   const int64_t blocks = std::min<int64_t>((n + 7) / 8, int64_t(num_sms) * 16);
   normalize_rows_kernel<<<static_cast<int>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(corpus, n, d, pitch);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_normalize_query(const float* q, int d, int pitch, float* out, cudaStream_t st) {
-  normalize_query_kernel<<<1, 32, 0, st>>>(q, d, pitch, out);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,16 @@ __device__ __forceinline__ int32_t ikey_value(uint64_t key) {
 __device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
+// 1 / sqrt(ss) for a sum of squares ss (cosine mode), or NaN when the norm is
+// zero or not finite: such a vector then scores NaN everywhere, which the
+// selection keys rank as -infinity.
+__device__ __forceinline__ double inv_l2_norm(double ss) {
+  return (ss > 0.0 && ss <= 1.7976931348623157e308) ? 1.0 / sqrt(ss) : __longlong_as_double(0x7FF8000000000000ll);
+}
+__device__ __forceinline__ float inv_l2_norm_f(float ss) {
+  return (ss > 0.0f && ss <= 3.402823466e38f) ? 1.0f / sqrtf(ss) : __int_as_float(0x7FC00000);
+}
+
 // ------------------------------------------------------- timers, mbarriers
 
 __device__ __forceinline__ uint64_t global_timer_ns() {

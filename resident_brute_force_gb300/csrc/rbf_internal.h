@@ -35,6 +35,7 @@ struct ScoreSelectLaunch {
   int grid;
   int dynamic;             // 0 = static contiguous row ranges, 1 = tile claims
   uint64_t timeout_ns;
+  int normalize_query = 0; // 1: score with the query scaled to unit length (cosine mode)
 };
 
 // Shared memory the fused kernel needs for a launch shape.
@@ -84,11 +85,10 @@ cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream
 
 cudaError_t launch_wait_probe(int* err, uint64_t timeout_ns, cudaStream_t stream);
 
-// Cosine mode: unit-length rows (in place, at upload), a unit-length copy of
-// one query (out: pitch floats, zero past d), and unit-length bf16 queries
-// for the batched path. A zero-norm vector becomes all NaN (scores -inf).
+// Cosine mode: unit-length rows (in place, at upload) and unit-length bf16
+// queries for the batched path. A zero-norm vector becomes all NaN (scores
+// -inf).
 cudaError_t launch_normalize_rows(float* corpus, int64_t n, int d, int pitch, int num_sms, cudaStream_t st);
-cudaError_t launch_normalize_query(const float* q, int d, int pitch, float* out, cudaStream_t st);
 cudaError_t launch_normalize_queries_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch,
                                           int64_t rows, int64_t rows_total, int cols, int num_sms, cudaStream_t st);
 

@@ -48,8 +48,9 @@ struct Params {
 };
 
 // NCH > 0: rows are exactly NCH * 128 floats and the query lives in
-// registers. NCH == 0: any pitch, query read from shared memory.
-template <int KP, int NCH>
+// registers. NCH == 0: any pitch, query read from shared memory. NORM:
+// cosine mode, the kernel first scales its copy of the query to unit length.
+template <int KP, int NCH, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Params p) {
   constexpr int R = KP / 32;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -76,6 +77,26 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
   }
   if constexpr (NCH == 0) {
     for (int i = threadIdx.x; i < p.pitch; i += blockDim.x) sq[i] = (i < p.d) ? p.query[i] : 0.0f;
+    if constexpr (NORM) {
+      // Cosine mode: the shared copy scaled to unit length (fp32 sum of
+      // squares in a fixed order, so every CTA gets the same bits).
+      __shared__ float s_part[NW + 1];
+      __shared__ float s_inv;
+      __syncthreads();
+      float ss = 0.0f;
+      for (int i = threadIdx.x; i < p.d; i += blockDim.x) ss = fmaf(sq[i], sq[i], ss);
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(kFullMask, ss, m);
+      if (lane == 0) s_part[warp] = ss;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = 0; w <= NW; ++w) t += s_part[w];
+        s_inv = inv_l2_norm_f(t);
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < p.d; i += blockDim.x) sq[i] *= s_inv;
+    }
   }
   __syncthreads();
 
@@ -160,6 +181,28 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
         q[j].y = (e + 1 < p.d) ? p.query[e + 1] : 0.0f;
         q[j].z = (e + 2 < p.d) ? p.query[e + 2] : 0.0f;
         q[j].w = (e + 3 < p.d) ? p.query[e + 3] : 0.0f;
+      }
+      if constexpr (NORM) {
+        // Cosine mode: every consumer warp scales its register copy to unit
+        // length (fp32 sum of squares, the same order in every warp).
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          ss = fmaf(q[j].x, q[j].x, ss);
+          ss = fmaf(q[j].y, q[j].y, ss);
+          ss = fmaf(q[j].z, q[j].z, ss);
+          ss = fmaf(q[j].w, q[j].w, ss);
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(kFullMask, ss, m);
+        const float inv = inv_l2_norm_f(ss);
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          q[j].x *= inv;
+          q[j].y *= inv;
+          q[j].z *= inv;
+          q[j].w *= inv;
+        }
       }
     }
     const float4* sq4 = reinterpret_cast<const float4*>(sq);
@@ -253,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
   }
 }
 
-template <int KP, int NCH>
+template <int KP, int NCH, bool NORM>
 cudaError_t launch_t(const Params& p, int grid, int smem, cudaStream_t stream) {
-  auto fn = score_select_f32_kernel<KP, NCH>;
+  auto fn = score_select_f32_kernel<KP, NCH, NORM>;
   static int configured = 0;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -266,14 +309,19 @@ cudaError_t launch_t(const Params& p, int grid, int smem, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int KP>
-cudaError_t launch_kp(const Params& p, int grid, int smem, cudaStream_t stream) {
+template <int KP, bool NORM>
+cudaError_t launch_kpn(const Params& p, int grid, int smem, cudaStream_t stream) {
   switch (p.pitch) {
-    case 384: return launch_t<KP, 3>(p, grid, smem, stream);
-    case 768: return launch_t<KP, 6>(p, grid, smem, stream);
-    case 1024: return launch_t<KP, 8>(p, grid, smem, stream);
-    default: return launch_t<KP, 0>(p, grid, smem, stream);
+    case 384: return launch_t<KP, 3, NORM>(p, grid, smem, stream);
+    case 768: return launch_t<KP, 6, NORM>(p, grid, smem, stream);
+    case 1024: return launch_t<KP, 8, NORM>(p, grid, smem, stream);
+    default: return launch_t<KP, 0, NORM>(p, grid, smem, stream);
   }
+}
+
+template <int KP>
+cudaError_t launch_kp(const Params& p, int grid, int smem, bool norm, cudaStream_t stream) {
+  return norm ? launch_kpn<KP, true>(p, grid, smem, stream) : launch_kpn<KP, false>(p, grid, smem, stream);
 }
 
 int region_bytes(int pitch, int k, int rows_per_stage, int stages) {
@@ -308,10 +356,10 @@ cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream)
   p.timeout_ns = a.timeout_ns;
   const int smem = score_select_smem_bytes(a.pitch, a.k, a.rows_per_stage, a.stages);
   switch (list_width(a.k)) {
-    case 32: return launch_kp<32>(p, a.grid, smem, stream);
-    case 64: return launch_kp<64>(p, a.grid, smem, stream);
-    case 128: return launch_kp<128>(p, a.grid, smem, stream);
-    case 256: return launch_kp<256>(p, a.grid, smem, stream);
+    case 32: return launch_kp<32>(p, a.grid, smem, a.normalize_query != 0, stream);
+    case 64: return launch_kp<64>(p, a.grid, smem, a.normalize_query != 0, stream);
+    case 128: return launch_kp<128>(p, a.grid, smem, a.normalize_query != 0, stream);
+    case 256: return launch_kp<256>(p, a.grid, smem, a.normalize_query != 0, stream);
     default: return cudaErrorInvalidValue;
   }
 }
