@@ -64,6 +64,19 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's).
+    A CPU tensor under gloo, a device tensor under NCCL."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -423,12 +436,7 @@ def main():
         barrier()
         step_ms = [bounds[j].elapsed_time(bounds[j + 1]) for j in range(args.steps)]
         k1_ms = [bounds[j].elapsed_time(mids[j]) for j in sorted(mids)]
-        total_ms = bounds[0].elapsed_time(bounds[args.steps])
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([total_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
+        total_ms = max_over_ranks(bounds[0].elapsed_time(bounds[args.steps]), world)
         rec = {
             "p50_us": round(percentile(step_ms, 50) * 1e3, 2),
             "p99_us": round(percentile(step_ms, 99) * 1e3, 2),
@@ -456,12 +464,7 @@ def main():
             t1 = time.perf_counter()
             eng.search_resident(qs[j % nq], 8)
             call_s.append(time.perf_counter() - t1)
-        dt = time.perf_counter() - t0
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([dt], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
+        dt = max_over_ranks(time.perf_counter() - t0, world)
         e2e = {"value": round(world * args.steps * bytes_per_step / dt / 1e9, 1), "unit": "GB/s",
                "h2d_bytes_per_step": d * 4, "d2h_bytes_per_step": result_d2h_bytes(8),
                "p50_us": round(percentile(call_s, 50) * 1e6, 2), "p99_us": round(percentile(call_s, 99) * 1e6, 2),
