@@ -79,6 +79,7 @@ struct rbf_engine {
   // Pinned host staging.
   uint8_t* h_query = nullptr;
   uint8_t* h_result = nullptr;
+  uint8_t* d_hres = nullptr;     // h_result as the device addresses it (pinned, mapped)
 
   // Options.
   int ctas_per_sm = 1;
@@ -224,8 +225,11 @@ ResultLayout result_layout(size_t count, size_t eb) {
   return r;
 }
 
+// The merge of a host-buffer call writes its results and the call's error
+// word straight into the pinned host block (no separate device-to-host copy),
+// so finishing the call is a stream synchronisation.
 rbf_status finish_host_call(rbf_engine* e, const ResultLayout& L) {
-  RBF_COPY(e, cudaMemcpyAsync(e->h_result, e->result, L.bytes, cudaMemcpyDeviceToHost, e->stream));
+  (void)L;
   cudaError_t st = cudaStreamSynchronize(e->stream);
   if (st != cudaSuccess) return cuda_fail(e, st);
   int derr = 0;
@@ -337,6 +341,7 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   ok = ok && cudaMalloc(&e->result, e->result_bytes) == cudaSuccess;
   ok = ok && cudaMallocHost(&e->h_query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMallocHost(&e->h_result, e->result_bytes) == cudaSuccess;
+  ok = ok && cudaHostGetDevicePointer(reinterpret_cast<void**>(&e->d_hres), e->h_result, 0) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     release(e);
@@ -476,8 +481,8 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
   RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
   if (rbf_status s = enqueue_score(e, e->query, k)) return s;
   const ResultLayout L = result_layout(static_cast<size_t>(k), 4);
-  if (rbf_status s = enqueue_merge(e, k, e->last_lists, 1, 0, reinterpret_cast<int32_t*>(e->result + L.a_off),
-                                   e->result + L.b_off, reinterpret_cast<int*>(e->result)))
+  if (rbf_status s = enqueue_merge(e, k, e->last_lists, 1, 0, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
+                                   e->d_hres + L.b_off, reinterpret_cast<int*>(e->d_hres)))
     return s;
   if (rbf_status s = finish_host_call(e, L)) return s;
   std::memcpy(out_idx, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
@@ -577,8 +582,8 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
   const size_t count = static_cast<size_t>(b) * k;
   const ResultLayout L = result_layout(count, 4);
-  if (rbf_status s = enqueue_batch(e, e->query, b, k, reinterpret_cast<int32_t*>(e->result + L.a_off),
-                                   reinterpret_cast<float*>(e->result + L.b_off), reinterpret_cast<int*>(e->result)))
+  if (rbf_status s = enqueue_batch(e, e->query, b, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
+                                   reinterpret_cast<float*>(e->d_hres + L.b_off), reinterpret_cast<int*>(e->d_hres)))
     return s;
   if (rbf_status s = finish_host_call(e, L)) return s;
   std::memcpy(out_idx, e->h_result + L.a_off, 4 * count);
@@ -669,9 +674,9 @@ rbf_status topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k
   if (rbf_status s = check_i32_args(e, d_data, n, k)) return s;
   if (!out_val || !out_pos) return RBF_ERR_INVALID_VALUE;
   const ResultLayout L = result_layout(static_cast<size_t>(k), 8);
-  if (rbf_status s = enqueue_topk_int32(e, d_data, n, k, reinterpret_cast<int32_t*>(e->result + L.a_off),
-                                        reinterpret_cast<int64_t*>(e->result + L.b_off),
-                                        reinterpret_cast<int*>(e->result)))
+  if (rbf_status s = enqueue_topk_int32(e, d_data, n, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
+                                        reinterpret_cast<int64_t*>(e->d_hres + L.b_off),
+                                        reinterpret_cast<int*>(e->d_hres)))
     return s;
   if (rbf_status s = finish_host_call(e, L)) return s;
   std::memcpy(out_val, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
