@@ -617,7 +617,7 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
   }
   // Large arrays: the bulk-copy ring kernel, one CTA per SM. Each CTA bounds
   // the K-th key from its own slice before its first tile. That bound weakens
-  // as K grows (it comes from 16,384 values), so for K >= kI32SampleMinK the
+  // as K grows (it comes from 32,768 values), so for K >= kI32SampleMinK the
   // exact K-th key of the first kI32SampleElems elements -- also a lower
   // bound, as they are part of the array -- is computed first and passed in.
   if (static_cast<size_t>(e->num_sms) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;

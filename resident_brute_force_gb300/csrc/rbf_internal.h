@@ -69,7 +69,7 @@ cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
 
 // Stage 1 for large arrays: bulk-copy ring, dynamic 64 KB tile claims, one
 // CTA of 16 consumer warps + 1 producer per SM; each CTA bounds the K-th key
-// from its own 16,384-value slice before its first tile. K <= 256.
+// from its own 32,768-value slice before its first tile. K <= 256.
 struct I32StreamLaunch {
   const int32_t* data;
   int64_t n;

@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
 // consumer warps scan each tile; one producer warp feeds the ring.
 //
 // Before the first tile each CTA takes a lower bound on the final K-th key
-// from its own slice of 16,384 values: the K-th largest of 256 group maxima
-// (groups of 64 values). K distinct groups each hold a key at least that
+// from its own slice of 32,768 values: the K-th largest of 256 group maxima
+// (groups of 128 values). K distinct groups each hold a key at least that
 // large, so at least K keys of the array are >= it and no key below it can be
 // in the top K. The consumers read the slice while the producer fills the
 // ring, and every key below the bound is dropped from the start. No CTA ever
@@ -200,8 +200,10 @@ constexpr int kSStages = 3;
 constexpr int kSTileVec = 4096;                 // int4 per tile (64 KB)
 constexpr int kSTileBytes = kSTileVec * 16;
 constexpr int kBoundGroups = 256;               // group maxima per slice (K <= 256)
-constexpr int kBoundVecPerThread = kSTileVec / (kSW * 32);  // 8 int4 = 32 values per thread
+constexpr int kBoundSliceVec = 2 * kSTileVec;   // int4 per slice (32,768 values)
+constexpr int kBoundVecPerThread = kBoundSliceVec / (kSW * 32);  // 16 int4 = 64 values per thread
 static_assert(kSW * 32 == 2 * kBoundGroups, "two consumer threads per group");
+static_assert(kBoundVecPerThread % 8 == 0, "slice loads go in batches of 8");
 
 struct StreamParams {
   const int32_t* data;
@@ -312,21 +314,25 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
       const uint64_t b0 = *p.theta0;
       floor_key = b0 > 0 ? b0 - 1 : 0;
     }
-    const int64_t slice = static_cast<int64_t>(blockIdx.x) * kSTileVec;
-    if (slice + kSTileVec <= nvec) {  // CTA-uniform: every consumer warp takes part
-      // Group g = threadIdx.x / 2 covers 16 vectors of the slice, 8 per thread,
-      // strided by 512 vectors so that every load is coalesced.
-      int4 x[kBoundVecPerThread];
-#pragma unroll
-      for (int j = 0; j < kBoundVecPerThread; ++j) x[j] = __ldcg(vec + slice + threadIdx.x + j * (kSW * 32));
+    const int64_t slice = static_cast<int64_t>(blockIdx.x) * kBoundSliceVec;
+    if (slice + kBoundSliceVec <= nvec) {  // CTA-uniform: every consumer warp takes part
+      // Group g = threadIdx.x / 2 covers 32 vectors of the slice, 16 per
+      // thread, strided by 512 vectors so that every load is coalesced (eight
+      // loads in flight at a time).
       uint64_t best = 0;
 #pragma unroll
-      for (int j = 0; j < kBoundVecPerThread; ++j) {
-        const uint32_t p0 = static_cast<uint32_t>(head + (slice + threadIdx.x + j * (kSW * 32)) * 4);
-        best = umax64(best, make_ikey(x[j].x, p0));
-        best = umax64(best, make_ikey(x[j].y, p0 + 1));
-        best = umax64(best, make_ikey(x[j].z, p0 + 2));
-        best = umax64(best, make_ikey(x[j].w, p0 + 3));
+      for (int j0 = 0; j0 < kBoundVecPerThread; j0 += 8) {
+        int4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = __ldcg(vec + slice + threadIdx.x + (j0 + j) * (kSW * 32));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t p0 = static_cast<uint32_t>(head + (slice + threadIdx.x + (j0 + j) * (kSW * 32)) * 4);
+          best = umax64(best, make_ikey(x[j].x, p0));
+          best = umax64(best, make_ikey(x[j].y, p0 + 1));
+          best = umax64(best, make_ikey(x[j].z, p0 + 2));
+          best = umax64(best, make_ikey(x[j].w, p0 + 3));
+        }
       }
       best = umax64(best, shfl_xor_u64(best, 1));
       uint64_t* gmax = reinterpret_cast<uint64_t*>(bufs);  // 256 keys, 2 KB

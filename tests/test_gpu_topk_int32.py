@@ -102,7 +102,7 @@ def test_full_size_1e8(eng):
 
 def test_sample_bound_cases(eng):
     """n >= 262,144: CTA b starts from a lower bound on the K-th key taken
-    from its own slice of 16,384 values (vectors 4096 b .. 4096 b + 4095 of
+    from its own slice of 32,768 values (vectors 8192 b .. 8192 b + 8191 of
     the 16-byte aligned body). Increasing arrays put every winner outside the
     early slices; constant arrays tie every key with the bound."""
     n = 600_000
@@ -126,8 +126,8 @@ def test_winners_inside_one_slice(eng, offset):
     n = 1_000_003
     rng = np.random.default_rng(8)
     x = workloads.int32_small_range(n + offset, seed=9, lo=-1000, hi=1000)
-    lo = offset + ((16 - (offset * 4) % 16) % 16) // 4 + 7 * 16384
-    hot = lo + rng.choice(16384, size=600, replace=False)
+    lo = offset + ((16 - (offset * 4) % 16) % 16) // 4 + 7 * 32768
+    hot = lo + rng.choice(32768, size=600, replace=False)
     x[hot] = INT32_MAX - rng.integers(0, 40, size=600).astype(np.int32)
     d = _dev(x)[offset:]
     for k in (1, 20, 50, 256):
