@@ -650,9 +650,13 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
   a.err = e->errw;
   a.grid = e->num_sms;
   a.timeout_ns = e->timeout_ns;
+  // Stage 2 runs in the kernel's last CTA.
+  a.out_val = val;
+  a.out_pos = pos;
+  a.err_sticky = e->errw + 1;
+  a.result_err = result_err;
   RBF_LAUNCH(e, launch_topk_i32_stream(a, e->stream));
-  lists = e->num_sms;
-  return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err);
+  return RBF_OK;
 }
 
 static rbf_status check_i32_args(const rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k) {

@@ -77,9 +77,15 @@ struct I32StreamLaunch {
   uint64_t* partials;          // grid lists of list_width(k) keys
   const uint64_t* theta0;      // optional lower bound on the K-th key (keys >= it are kept)
   unsigned* counters;          // 2 words, zero between launches
-  int* err;
+  int* err;                    // per-call error word
   int grid;
   uint64_t timeout_ns;
+  // Optional stage 2 in the kernel's last CTA: K values and positions, and
+  // the per-call error word handed to result_err / err_sticky (then cleared).
+  int32_t* out_val = nullptr;
+  int64_t* out_pos = nullptr;
+  int* err_sticky = nullptr;
+  int* result_err = nullptr;
 };
 cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream);
 

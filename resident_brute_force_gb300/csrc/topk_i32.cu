@@ -15,6 +15,7 @@
 //   * the few elements before the first 16-byte boundary and after the last
 //     one are handled by scalar loads in CTA 0;
 //   * the CTA merges its warps' lists and writes one best-first list.
+#include "merge_core.cuh"
 #include "rbf_device.cuh"
 #include "rbf_internal.h"
 
@@ -214,7 +215,18 @@ struct StreamParams {
   unsigned* counters;  // [0] tile claims, [1] finished CTAs; zero between launches
   int* err;
   uint64_t timeout_ns;
+  // Merge in the last CTA (when out_val is set): the K values and positions,
+  // and the per-call error word handed to result_err / err_sticky.
+  int32_t* out_val;
+  int64_t* out_pos;
+  int* err_sticky;
+  int* result_err;
 };
+
+// The last CTA merges in the ring's shared memory (the barriers after it are
+// left alone).
+constexpr int kMergeSmemBytes = kSStages * kSTileBytes;
+constexpr int kMergeStageKeys = (kMergeSmemBytes / 8 - mergecore::kSurvivorCap - 2) & ~1;
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kSW * 32) : "memory"); }
 
@@ -421,13 +433,37 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     __syncthreads();
   }
   if (warp == 0) warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
+  __shared__ int s_last;
+  __threadfence();  // this CTA's list is visible before its ticket
+  __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
     const unsigned done = atomicAdd(&p.counters[1], 1u);
-    if (done == gridDim.x - 1) {
+    s_last = done == gridDim.x - 1 ? 1 : 0;
+    if (s_last) {
       atomicExch(&p.counters[0], 0u);
       atomicExch(&p.counters[1], 0u);
-      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (s_last && p.out_val) {
+    // Stage 2 in the last CTA to finish: every other CTA's list is written.
+    __threadfence();
+    mergecore::MergeOut o;
+    o.k = p.k;
+    o.int_keys = 1;
+    o.out_a = p.out_val;
+    o.out_b = p.out_pos;
+    o.kth_out = nullptr;
+    o.q = 0;
+    mergecore::merge_lists<KP, kSThreads>(o, p.partials, static_cast<int>(gridDim.x),
+                                          reinterpret_cast<uint64_t*>(smem), kMergeSmemBytes, kMergeStageKeys);
+    if (threadIdx.x == 0) {
+      // Hand the per-call error word to the host-visible result and the
+      // sticky word, then re-arm it for the next call.
+      const int e = atomicOr(p.err, 0);
+      if (p.result_err) *p.result_err = e;
+      if (e && p.err_sticky) atomicOr(p.err_sticky, e);
+      atomicExch(p.err, 0);
     }
   }
 }
@@ -487,6 +523,10 @@ cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream
   p.counters = a.counters;
   p.err = a.err;
   p.timeout_ns = a.timeout_ns;
+  p.out_val = a.out_val;
+  p.out_pos = a.out_pos;
+  p.err_sticky = a.err_sticky;
+  p.result_err = a.result_err;
   if (a.k < 1 || a.k > kBoundGroups) return cudaErrorInvalidValue;
   switch (list_width(a.k)) {
     case 32: return launch_stream_t<32>(p, a.grid, stream);
