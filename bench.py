@@ -262,9 +262,13 @@ def time_device(stream, fn, steps, warmup):
     return [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
 
 
-def run_batched(rbf, steps, warmup):
-    """Batched queries: B=256 x N=1,000,000 x D=768, bf16 corpus, fp32
-    accumulate, K=32 (tensor-core scoring + fused select + merge)."""
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates
+
+
+def run_batched(rbf, steps, warmup, tf32=False):
+    """Batched queries: B=256 x N=1,000,000 x D=768, K=32 (tensor-core scoring
+    + fused select + merge), fp32 accumulate; bf16 corpus copy, or with
+    tf32=True the resident fp32 corpus itself (kind::tf32)."""
     import torch
     import workloads
     n, d, b, k = 1_000_000, 768, 256, 32
@@ -272,7 +276,7 @@ def run_batched(rbf, steps, warmup):
     qs = workloads.unit_queries(b, d, seed=2)
     workloads.plant_near_duplicates(c, qs, per_query=10, noise=0.05, seed=3)
     st = torch.cuda.Stream()
-    e = rbf.Engine(n, d, k, max_batch=b, flags=rbf.RBF_FLAG_BF16_CORPUS, stream=st)
+    e = rbf.Engine(n, d, k, max_batch=b, flags=0 if tf32 else rbf.RBF_FLAG_BF16_CORPUS, stream=st)
     e.upload_corpus_rowmajor(c)
     del c
     dq = torch.from_numpy(qs).cuda()
@@ -283,12 +287,15 @@ def run_batched(rbf, steps, warmup):
     p50 = percentile(ms, 50) * 1e-3
     flops = 2.0 * b * n * d
     peak, src = bf16_peak()
+    if tf32:
+        peak, src = round(peak * TF32_OVER_BF16, 1), src + " bf16 x nominal tf32/bf16 ratio"
     hbm, hsrc = hbm_peak()
-    corpus_bytes = n * d * 2
+    corpus_bytes = n * d * (4 if tf32 else 2)
     # Both rooflines: the tensor work at the bf16 peak and the one pass over
     # the bf16 corpus at the HBM peak; the slower of the two bounds the call.
     bound = "hbm" if corpus_bytes / (hbm * 1e9) > flops / (peak * 1e12) else "tensor"
-    return {"workload": "B=256 x N=1,000,000 x D=768 bf16 corpus (fp32 accumulate), K=32, 10 planted rows/query",
+    corpus = "fp32 corpus as tf32" if tf32 else "bf16 corpus"
+    return {"workload": f"B=256 x N=1,000,000 x D=768 {corpus} (fp32 accumulate), K=32, 10 planted rows/query",
             "p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
             "tflops": round(flops / p50 / 1e12, 1), "tensor_peak_tflops": peak, "peak_source": src,
             "tensor_frac": round(flops / p50 / 1e12 / peak, 4),
@@ -483,6 +490,7 @@ def main():
     eng.close()
     cosine = run_cosine(rbf, c, qs, planted, 200, 5) if (rank == 0 and not args.no_cosine) else None
     batched = run_batched(rbf, 30, 3) if (rank == 0 and not args.no_batched) else None
+    batched_tf32 = run_batched(rbf, 20, 3, tf32=True) if (rank == 0 and not args.no_batched) else None
     int32 = run_int32(rbf, 50, 5) if (rank == 0 and not args.no_int32) else None
 
     cpu = None
@@ -508,6 +516,8 @@ def main():
             line["cosine"] = cosine
         if batched is not None:
             line["batched"] = batched
+        if batched_tf32 is not None:
+            line["batched_tf32"] = batched_tf32
         if int32 is not None:
             line["int32"] = int32
         print(json.dumps(line), flush=True)

@@ -59,7 +59,7 @@ typedef enum rbf_status {
 
 /* rbf_create flags. 0 means RBF_FLAG_FP32_CORPUS. */
 #define RBF_FLAG_FP32_CORPUS 0x1u /* keep the fp32 corpus: single-query path */
-#define RBF_FLAG_BF16_CORPUS 0x2u /* also keep a bf16 copy: batched path */
+#define RBF_FLAG_BF16_CORPUS 0x2u /* also keep a bf16 copy for the batched path (else it runs tf32) */
 /* Score by cosine similarity instead of the inner product: the inner product
  * divided by the product of the query's and the row's L2 norms, and -infinity
  * for a row whose denominator is not positive (GPU-Resident Top-K for Agentic
@@ -168,16 +168,21 @@ rbf_status merge_partial_topk_dev(rbf_engine* engine, int32_t k, int32_t* d_idx,
 
 /* ---------------------------------------------------------------- batched */
 
-/* Top-K of each of B queries (row-major B x D) against the resident corpus.
- * Needs RBF_FLAG_BF16_CORPUS: scores are bf16 x bf16 products (queries are
- * rounded to bf16 on the device) accumulated in fp32 on the tensor cores.
+/* Top-K of each of B queries (row-major B x D) against the resident corpus,
+ * with the scoring on the tensor cores and the selection fused into their
+ * epilogue (the same per-block partial top-K and merge as the single-query
+ * path, GPU-Resident Top-K for Agentic RAG, section 4 steps 2-4). With
+ * RBF_FLAG_BF16_CORPUS scores are bf16 x bf16 products (queries rounded to
+ * bf16 on the device) accumulated in fp32; without it the resident fp32
+ * corpus and fp32 queries are multiplied as tf32 (10-bit mantissas),
+ * accumulated in fp32.
  *   queries    host, B x D floats
  *   b          1 .. max_batch
- *   k          1 .. min(max_k, N)
+ *   k          1 .. min(max_k, N, 32)
  *   out_idx    host, B x K int32 (row q holds query q's list, best-first)
  *   out_score  host, B x K fp32
- * Errors: INVALID_VALUE, NOT_READY, UNSUPPORTED (no bf16 corpus), CUDA,
- * TIMEOUT. */
+ * Errors: INVALID_VALUE, NOT_READY, UNSUPPORTED (k > 32: the fused select
+ * keeps 32 keys per query and CTA), CUDA, TIMEOUT. */
 rbf_status search_resident_batch(rbf_engine* engine, const float* queries, int32_t b, int32_t k,
                                  int32_t* out_idx, float* out_score);
 

@@ -58,6 +58,7 @@ struct rbf_engine {
   // bf16 copies for the batched path (RBF_FLAG_BF16_CORPUS).
   void* corpus_bf16 = nullptr;   // tile-major, max_n rounded up to 128 rows x max_pitch_bf16
   void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
+  float* query_f32 = nullptr;    // tf32 batched path (no bf16 copy): query_rows x max_pitch floats
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
@@ -244,6 +245,7 @@ void release(rbf_engine* e) {
   cudaFree(e->corpus);
   cudaFree(e->corpus_bf16);
   cudaFree(e->query_bf16);
+  cudaFree(e->query_f32);
   cudaFree(e->theta0);
   cudaFree(e->query);
   cudaFree(e->partials);
@@ -313,13 +315,15 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   const size_t kpmax = static_cast<size_t>(list_width(max_k));
   const size_t max_lists = static_cast<size_t>(e->num_sms) * kMaxCtasPerSm;
   e->partials_cap = max_lists * kpmax;
+  // Batched search: on the bf16 copy when there is one, else (tf32) on the
+  // fp32 corpus itself.
+  e->query_rows = static_cast<int>(align_up(static_cast<size_t>(max_batch), kBatchQueriesPerLaunch));
+  const size_t batch_keys = static_cast<size_t>(max_batch) * e->num_sms * kBatchListWidth;
+  e->partials_cap = std::max(e->partials_cap, batch_keys);
   if (flags & RBF_FLAG_BF16_CORPUS) {
     flags |= RBF_FLAG_FP32_CORPUS;  // uploads are converted from the fp32 copy
     e->flags = flags;
     e->max_pitch_bf16 = static_cast<int>(align_up(static_cast<size_t>(max_d), kBf16PitchAlign));
-    e->query_rows = static_cast<int>(align_up(static_cast<size_t>(max_batch), kBatchQueriesPerLaunch));
-    const size_t batch_keys = static_cast<size_t>(max_batch) * e->num_sms * kBatchListWidth;
-    e->partials_cap = std::max(e->partials_cap, batch_keys);
   }
   const size_t result_count = static_cast<size_t>(max_batch) * max_k;
   e->result_bytes = result_layout(result_count, 8).bytes;
@@ -331,8 +335,10 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
     ok = ok && cudaMalloc(&e->corpus_bf16, align_up(static_cast<size_t>(max_n), 128) * e->max_pitch_bf16 * 2) ==
                    cudaSuccess;
     ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
-    ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
+  } else {
+    ok = ok && cudaMalloc(&e->query_f32, static_cast<size_t>(e->query_rows) * e->max_pitch * 4) == cudaSuccess;
   }
+  ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
@@ -438,6 +444,15 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
     }
     e->pitch_bf16 = pb;
     e->tmaps_ready = true;
+  } else {
+    // tf32 batched path: tensor maps over the resident fp32 corpus and the
+    // padded fp32 query buffer.
+    if (!make_f32_tensor_map(&e->tmap_corpus, e->corpus, n, pitch) ||
+        !make_f32_tensor_map(&e->tmap_query, e->query_f32, e->query_rows, pitch)) {
+      e->tmaps_ready = false;
+      return RBF_ERR_CUDA;
+    }
+    e->tmaps_ready = true;
   }
   cudaError_t st = cudaStreamSynchronize(e->stream);
   if (st != cudaSuccess) return cuda_fail(e, st);
@@ -494,11 +509,14 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
 // epilogue select once per group of up to 256 queries, merge every query.
 static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, int k, int32_t* d_idx, float* d_score,
                                 int* result_err) {
-  if (!e->corpus_bf16) return RBF_ERR_UNSUPPORTED;
   if (k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
   if (!e->tmaps_ready) return RBF_ERR_NOT_READY;
   const int64_t rows_total = static_cast<int64_t>(align_up(static_cast<size_t>(b), 128));
-  if (e->flags & RBF_FLAG_COSINE) {
+  const bool tf32 = e->corpus_bf16 == nullptr;
+  if (tf32) {
+    RBF_LAUNCH(e, launch_stage_queries_f32(d_queries, e->d, e->query_f32, e->pitch, b, rows_total, e->d,
+                                           (e->flags & RBF_FLAG_COSINE) != 0, e->num_sms, e->stream));
+  } else if (e->flags & RBF_FLAG_COSINE) {
     RBF_LAUNCH(e, launch_normalize_queries_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d,
                                                 e->num_sms, e->stream));
   } else {
@@ -520,7 +538,8 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
       a.partials = e->partials;
       a.err = e->errw;
       a.n = rows;
-      a.pitch_bf16 = e->pitch_bf16;
+      a.kchunks = tf32 ? (e->d + 31) / 32 : e->pitch_bf16 / 64;
+      a.tf32 = tf32 ? 1 : 0;
       a.q_row0 = q0;
       a.q_count = std::min(kBatchQueriesPerLaunch, b - q0);
       a.q_out0 = q0;
@@ -576,7 +595,7 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (!e || !queries || !out_idx || !out_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
-  if (!e->corpus_bf16 || k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
+  if (k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
   const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
   std::memcpy(e->h_query, queries, qbytes);
   RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));

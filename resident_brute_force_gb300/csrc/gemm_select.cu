@@ -36,6 +36,8 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kTileRows = 128;      // corpus rows per tile (MMA N)
 constexpr int kKChunk = 64;         // bf16 elements per 128-byte swizzle row
+constexpr int kKChunkTf32 = 32;     // fp32 (tf32) elements per 128-byte swizzle row
+constexpr int kMmaPerChunk = 4;     // MMAs per 128-byte row: K = 16 bf16 or 8 tf32, 32 bytes each
 constexpr int kSubTileBytes = 128 * kKChunk * 2;  // 16 KB: 128 rows x 128 B
 constexpr int kStageBytes = 3 * kSubTileBytes;    // A0 | A1 | B
 constexpr int kCandCap = 16;        // buffered candidates per query
@@ -59,15 +61,26 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D(tmem) (+)= A(smem) * B(smem)^T, both K-major bf16, fp32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// D(tmem) (+)= A(smem) * B(smem)^T, both K-major, fp32 accumulate: bf16
+// operands (kind::f16) or fp32 operands taken as tf32 (kind::tf32).
+template <bool TF32>
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  if constexpr (TF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
@@ -147,13 +160,20 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(const void* tile) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
-// bf16 (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at
-// bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+// Instruction descriptor: fp32 accumulator (bits 4-5 = 1), the A and B
+// formats (bits 7-9 and 10-12: 1 = bf16 for kind::f16, 2 = tf32 for
+// kind::tf32), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
+
+// Elements of one 64 x 128-byte K chunk and the operand format code.
+template <bool TF32>
+struct Operand {
+  static constexpr int kChunk = TF32 ? kKChunkTf32 : kKChunk;
+  static constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+};
 
 // ------------------------------------------------- per-thread key lists
 
@@ -227,7 +247,7 @@ struct Params {
   int* err;
   int64_t n;           // corpus rows
   int num_tiles;       // ceil(n / 128)
-  int kchunks;         // padded D / 64
+  int kchunks;         // 128-byte K chunks per row (64 bf16 or 32 fp32 elements)
   int num_mt;          // 1 or 2 M tiles of 128 queries in this launch
   int q_row0;          // first query row of this launch in the bf16 query buffer
   int q_count;         // queries in this launch
@@ -238,10 +258,11 @@ struct Params {
   int bound_mode;          // 1: write the best key of each 32-row chunk instead of a top-K list
 };
 
-template <int KP>
+template <int KP, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_select_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
-                            const Params p) {
+    gemm_select_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
+                       const Params p) {
+  constexpr int CH = Operand<TF32>::kChunk;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -303,9 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(st, &tmap_q, kc * kKChunk, p.q_row0, &full[s], pol_q);
-          if (p.num_mt > 1) tma_load_2d(st + kSubTileBytes, &tmap_q, kc * kKChunk, p.q_row0 + 128, &full[s], pol_q);
-          tma_load_3d(st + 2 * kSubTileBytes, &tmap_c, 0, 0, t * p.kchunks + kc, &full[s], pol_c);
+          tma_load_2d(st, &tmap_q, kc * CH, p.q_row0, &full[s], pol_q);
+          if (p.num_mt > 1) tma_load_2d(st + kSubTileBytes, &tmap_q, kc * CH, p.q_row0 + 128, &full[s], pol_q);
+          if constexpr (TF32)  // the fp32 corpus, row-major
+            tma_load_2d(st + 2 * kSubTileBytes, &tmap_c, kc * CH, t * kTileRows, &full[s], pol_c);
+          else  // the tile-major bf16 copy: one contiguous 16 KB block
+            tma_load_3d(st + 2 * kSubTileBytes, &tmap_c, 0, 0, t * p.kchunks + kc, &full[s], pol_c);
         }
       }
       if (aborted) {
@@ -322,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(128, kTileRows);
+      constexpr uint32_t idesc = make_idesc(128, kTileRows, Operand<TF32>::kFmt);
       int64_t it = 0;
       int tile_i = 0;
       bool aborted = false;
@@ -351,10 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t adesc = sw128_kmajor_desc(st + m * kSubTileBytes);
               const uint32_t d = tmem_base + static_cast<uint32_t>(b * 256 + m * 128);
 #pragma unroll
-              for (int k = 0; k < kKChunk / 16; ++k) {
-                // Advance both descriptors 32 bytes (16 bf16) along K.
-                umma_bf16(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
-                          (kc | k) != 0);
+              for (int k = 0; k < kMmaPerChunk; ++k) {
+                // Advance both descriptors 32 bytes (16 bf16 or 8 tf32) along K.
+                umma<TF32>(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                           (kc | k) != 0);
               }
             }
           }
@@ -583,14 +607,24 @@ __device__ __forceinline__ void tmem_relinquish_pair() {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+template <bool TF32>
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (TF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 // Arrive once on `bar` in both CTAs of the pair when every MMA issued so far
 // is done.
@@ -620,10 +654,11 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-template <int KP>
+template <int KP, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_select_pair_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
                             const Params p) {
+  constexpr int CH = Operand<TF32>::kChunk;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -691,9 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = ring + static_cast<size_t>(s) * kPairStageBytes;
           if (leader) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * kPairStageBytes));
           const uint32_t bar = cluster_addr(&full[s], 0);
-          tma_load_2d_pair(st, &tmap_q, kc * kKChunk, p.q_row0 + static_cast<int>(rank) * 128, bar, pol_q);
-          tma_load_3d_pair(st + kSubTileBytes, &tmap_c, 0, 0, (2 * t + static_cast<int>(rank)) * p.kchunks + kc, bar,
-                           pol_c);
+          tma_load_2d_pair(st, &tmap_q, kc * CH, p.q_row0 + static_cast<int>(rank) * 128, bar, pol_q);
+          if constexpr (TF32)
+            tma_load_2d_pair(st + kSubTileBytes, &tmap_c, kc * CH, (2 * t + static_cast<int>(rank)) * kTileRows, bar,
+                             pol_c);
+          else
+            tma_load_3d_pair(st + kSubTileBytes, &tmap_c, 0, 0, (2 * t + static_cast<int>(rank)) * p.kchunks + kc, bar,
+                             pol_c);
         }
       }
       if (aborted) {
@@ -714,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       if (leader) {
-        constexpr uint32_t idesc = make_idesc(256, kPairTileRows);
+        constexpr uint32_t idesc = make_idesc(256, kPairTileRows, Operand<TF32>::kFmt);
         int64_t it = 0;
         int tile_i = 0;
         bool aborted = false;
@@ -740,9 +779,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = sw128_kmajor_desc(st + kSubTileBytes);
             const uint32_t d = tmem_base + static_cast<uint32_t>(b * kPairTileRows);
 #pragma unroll
-            for (int k = 0; k < kKChunk / 16; ++k)
-              umma_bf16_pair(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
-                             (kc | k) != 0);
+            for (int k = 0; k < kMmaPerChunk; ++k)
+              umma_pair<TF32>(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
+                              (kc | k) != 0);
             umma_commit_pair(&empty[s]);  // both CTAs' stage s is free once these MMAs finish
           }
           if (aborted) break;
@@ -878,9 +917,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int KP>
+template <int KP, bool TF32>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
-  auto fn = gemm_select_bf16_kernel<KP>;
+  auto fn = gemm_select_kernel<KP, TF32>;
   const int smem = gemm_select_smem_bytes();
   static int configured = 0;
   if (smem > configured) {
@@ -896,9 +935,9 @@ int pair_smem_bytes() {
   return 1024 + kPairStages * kPairStageBytes + kCandCap * 256 * 8 + (2 * kPairStages + 5) * 8 + 16;
 }
 
-template <int KP>
+template <int KP, bool TF32>
 cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
-  auto fn = gemm_select_pair_kernel<KP>;
+  auto fn = gemm_select_pair_kernel<KP, TF32>;
   const int smem = pair_smem_bytes();
   static int configured = 0;
   if (smem > configured) {
@@ -1001,6 +1040,19 @@ cudaError_t launch_to_bf16_tiled(const float* src, int64_t src_pitch, void* dst,
   return cudaGetLastError();
 }
 
+bool make_f32_tensor_map(void* map_out, const void* base, int64_t rows, int pitch_elems) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pitch_elems), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKChunkTf32), 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,
                            int64_t rows_total, int cols, int num_sms, cudaStream_t st) {
   const int64_t total = rows_total * dst_pitch;
@@ -1012,13 +1064,35 @@ cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64
   return cudaGetLastError();
 }
 
+template <bool TF32>
+cudaError_t launch_typed(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, const GemmSelectLaunch& a,
+                         cudaStream_t stream) {
+  if (a.bound_mode) {
+    // Bound mode writes 4 keys per tile and query: one tile per CTA.
+    if (p.num_tiles > a.grid) return cudaErrorInvalidValue;
+    return launch_t<8, TF32>(tq, tc, p, a.grid, stream);
+  }
+  if (a.grid < 2 || a.grid % 2 != 0) return cudaErrorInvalidValue;
+  if (a.q_count > 128) {
+    // Two M tiles: a CTA pair per 256-row tile (lists per query = grid).
+    if (a.k <= 8) return launch_pair_t<8, TF32>(tq, tc, p, a.grid, stream);
+    if (a.k <= 16) return launch_pair_t<16, TF32>(tq, tc, p, a.grid, stream);
+    if (a.k <= 32) return launch_pair_t<32, TF32>(tq, tc, p, a.grid, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (a.k <= 8) return launch_t<8, TF32>(tq, tc, p, a.grid, stream);
+  if (a.k <= 16) return launch_t<16, TF32>(tq, tc, p, a.grid, stream);
+  if (a.k <= 32) return launch_t<32, TF32>(tq, tc, p, a.grid, stream);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   Params p;
   p.partials = a.partials;
   p.err = a.err;
   p.n = a.n;
   p.num_tiles = static_cast<int>((a.n + kTileRows - 1) / kTileRows);
-  p.kchunks = a.pitch_bf16 / kKChunk;
+  p.kchunks = a.kchunks;
   p.num_mt = a.q_count > 128 ? 2 : 1;
   p.q_row0 = a.q_row0;
   p.q_count = a.q_count;
@@ -1027,26 +1101,9 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.timeout_ns = a.timeout_ns;
   p.theta0 = a.theta0;
   p.bound_mode = a.bound_mode;
-  if (a.bound_mode) {
-    // Bound mode writes 4 keys per tile and query: one tile per CTA.
-    if (p.num_tiles > a.grid) return cudaErrorInvalidValue;
-    return launch_t<8>(*static_cast<const CUtensorMap*>(a.tmap_q), *static_cast<const CUtensorMap*>(a.tmap_c), p,
-                       a.grid, stream);
-  }
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
-  if (a.grid < 2 || a.grid % 2 != 0) return cudaErrorInvalidValue;
-  if (a.q_count > 128) {
-    // Two M tiles: a CTA pair per 256-row tile (lists per query = grid).
-    if (a.k <= 8) return launch_pair_t<8>(tq, tc, p, a.grid, stream);
-    if (a.k <= 16) return launch_pair_t<16>(tq, tc, p, a.grid, stream);
-    if (a.k <= 32) return launch_pair_t<32>(tq, tc, p, a.grid, stream);
-    return cudaErrorInvalidValue;
-  }
-  if (a.k <= 8) return launch_t<8>(tq, tc, p, a.grid, stream);
-  if (a.k <= 16) return launch_t<16>(tq, tc, p, a.grid, stream);
-  if (a.k <= 32) return launch_t<32>(tq, tc, p, a.grid, stream);
-  return cudaErrorInvalidValue;
+  return a.tf32 ? launch_typed<true>(tq, tc, p, a, stream) : launch_typed<false>(tq, tc, p, a, stream);
 }
 
 }  // namespace rbf

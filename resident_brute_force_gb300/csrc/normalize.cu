@@ -67,7 +67,46 @@ __global__ void normalize_queries_bf16_kernel(const float* __restrict__ src, int
   }
 }
 
+// fp32 queries into a padded fp32 buffer for the tf32 batched path: one warp
+// per row, zero past `cols` and for rows in [rows, rows_total); with NORM the
+// row is scaled to unit length first (cosine mode).
+template <bool NORM>
+__global__ void stage_queries_f32_kernel(const float* __restrict__ src, int64_t src_pitch, float* __restrict__ dst,
+                                         int64_t dst_pitch, int64_t rows, int64_t rows_total, int cols) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows_total;
+       r += warps) {
+    float* o = dst + r * dst_pitch;
+    if (r < rows) {
+      const float* x = src + r * src_pitch;
+      double inv = 1.0;
+      if constexpr (NORM) inv = inv_l2_norm(warp_sumsq(x, cols, lane));
+      for (int64_t j = lane; j < dst_pitch; j += 32) {
+        if constexpr (NORM)
+          o[j] = j < cols ? static_cast<float>(static_cast<double>(x[j]) * inv) : 0.0f;
+        else
+          o[j] = j < cols ? x[j] : 0.0f;
+      }
+    } else {
+      for (int64_t j = lane; j < dst_pitch; j += 32) o[j] = 0.0f;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_stage_queries_f32(const float* src, int64_t src_pitch, float* dst, int64_t dst_pitch, int64_t rows,
+                                     int64_t rows_total, int cols, bool normalize, int num_sms, cudaStream_t st) {
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((rows_total + 7) / 8, int64_t(num_sms) * 4));
+  if (normalize)
+    stage_queries_f32_kernel<true><<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, dst, dst_pitch, rows,
+                                                                           rows_total, cols);
+  else
+    stage_queries_f32_kernel<false><<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, dst, dst_pitch, rows,
+                                                                            rows_total, cols);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_normalize_rows(float* corpus, int64_t n, int d, int pitch, int num_sms, cudaStream_t st) {
   const int64_t blocks = std::min<int64_t>((n + 7) / 8, int64_t(num_sms) * 16);

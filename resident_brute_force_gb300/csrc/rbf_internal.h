@@ -111,7 +111,8 @@ struct GemmSelectLaunch {
   uint64_t* partials;        // [queries][grid][32] keys
   int* err;
   int64_t n;                 // corpus rows
-  int pitch_bf16;            // padded D, a multiple of 64
+  int kchunks;               // 128-byte K chunks per row (64 bf16 or 32 fp32 elements each)
+  int tf32 = 0;              // 1: fp32 operands, kind::tf32 (tmap_c over the row-major fp32 corpus)
   int q_row0;                // first query row of this launch in the query buffer
   int q_count;               // queries in this launch, 1..256
   int q_out0;                // first query of this launch in the partials layout
@@ -125,6 +126,13 @@ struct GemmSelectLaunch {
 int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
 bool make_bf16_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);
+// Tensor map over a [rows][pitch] fp32 matrix: 32 x 128 boxes, 128-byte swizzle
+// (the tf32 batched path: the resident corpus and the padded queries).
+bool make_f32_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);
+// fp32 queries [rows][src_pitch] -> [rows_total][dst_pitch] fp32, zero-padded,
+// optionally scaled to unit length (cosine mode).
+cudaError_t launch_stage_queries_f32(const float* src, int64_t src_pitch, float* dst, int64_t dst_pitch, int64_t rows,
+                                     int64_t rows_total, int cols, bool normalize, int num_sms, cudaStream_t st);
 // Corpus copy for the batched path, tile-major: [ceil(rows/128)][pitch/64][128][64]
 // bf16, rows past `rows` zero. The map's box is one 16 KB block.
 bool make_bf16_tiled_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);

@@ -94,11 +94,6 @@ def test_dev_matches_host_and_repeats(rbf):
 def test_unsupported_and_invalid(rbf):
     c = workloads.dyadic_grid(500, 64, seed=21)
     qs = workloads.dyadic_grid(4, 64, seed=22)
-    with rbf.Engine(500, 64, 64, max_batch=4) as e:      # no bf16 copy
-        e.upload_corpus_rowmajor(c)
-        with pytest.raises(rbf.RbfError) as ei:
-            e.search_resident_batch(qs, 8)
-        assert ei.value.status == rbf.RBF_ERR_UNSUPPORTED
     with engine(rbf, 500, 64, 4, k=64) as e:
         e.upload_corpus_rowmajor(c)
         with pytest.raises(rbf.RbfError) as ei:
