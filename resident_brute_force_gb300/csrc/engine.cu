@@ -81,6 +81,10 @@ struct rbf_engine {
   uint8_t* h_query = nullptr;
   uint8_t* h_result = nullptr;
   uint8_t* d_hres = nullptr;     // h_result as the device addresses it (pinned, mapped)
+  // search_resident as one CUDA graph per K (query copy, scoring, merge),
+  // captured on first use and dropped whenever the corpus or an option changes.
+  cudaGraphExec_t host_graph[RBF_MAX_K + 1] = {};
+  int host_graph_lists[RBF_MAX_K + 1] = {};
 
   // Options.
   int ctas_per_sm = 1;
@@ -239,9 +243,17 @@ rbf_status finish_host_call(rbf_engine* e, const ResultLayout& L) {
   return RBF_OK;
 }
 
+void drop_graphs(rbf_engine* e) {
+  for (auto& g : e->host_graph) {
+    if (g) cudaGraphExecDestroy(g);
+    g = nullptr;
+  }
+}
+
 void release(rbf_engine* e) {
   if (!e) return;
   if (e->stream) cudaStreamSynchronize(e->stream);
+  drop_graphs(e);
   cudaFree(e->corpus);
   cudaFree(e->corpus_bf16);
   cudaFree(e->query_bf16);
@@ -385,6 +397,8 @@ int32_t rbf_last_cuda_error(const rbf_engine* e) { return e ? e->last_cuda_error
 
 rbf_status rbf_set_option(rbf_engine* e, rbf_option opt, int64_t value) {
   if (!e) return RBF_ERR_INVALID_VALUE;
+  cudaStreamSynchronize(e->stream);
+  drop_graphs(e);  // captured launches carry the old launch shape
   switch (opt) {
     case RBF_OPT_CTAS_PER_SM:
       if (value < 1 || value > kMaxCtasPerSm) return RBF_ERR_INVALID_VALUE;
@@ -425,6 +439,8 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
   if (!e || !corpus || n < 1 || n > e->max_n || d < 1 || d > e->max_d) return RBF_ERR_INVALID_VALUE;
   if (!e->corpus) return RBF_ERR_UNSUPPORTED;
   e->ready = false;
+  cudaStreamSynchronize(e->stream);
+  drop_graphs(e);  // captured launches carry the old corpus shape
   const int pitch = static_cast<int>(align_up(static_cast<size_t>(d), 4));
   RBF_COPY(e, cudaMemcpy2DAsync(e->corpus, static_cast<size_t>(pitch) * 4, corpus, static_cast<size_t>(d) * 4,
                                 static_cast<size_t>(d) * 4, static_cast<size_t>(n), cudaMemcpyDefault, e->stream));
@@ -487,18 +503,54 @@ rbf_status search_resident_dev(rbf_engine* e, const float* d_query, int32_t k, i
   return enqueue_merge(e, k, e->last_lists, 1, 0, d_idx, d_score, reinterpret_cast<int*>(e->result));
 }
 
+// The device work of one search_resident call: query copy from the pinned
+// staging buffer, scoring, merge into the pinned result block.
+static rbf_status enqueue_host_search(rbf_engine* e, int k, const ResultLayout& L) {
+  const size_t qbytes = static_cast<size_t>(e->d) * 4;
+  RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
+  if (rbf_status s = enqueue_score(e, e->query, k)) return s;
+  return enqueue_merge(e, k, e->last_lists, 1, 0, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
+                       e->d_hres + L.b_off, reinterpret_cast<int*>(e->d_hres));
+}
+
+// Record enqueue_host_search for this K as a CUDA graph (one launch per
+// call afterwards). Nothing is cached if anything fails.
+static rbf_status capture_host_search(rbf_engine* e, int k, const ResultLayout& L) {
+  cudaError_t st = cudaStreamBeginCapture(e->stream, cudaStreamCaptureModeRelaxed);
+  if (st != cudaSuccess) return cuda_fail(e, st);
+  const rbf_status s = enqueue_host_search(e, k, L);
+  cudaGraph_t graph = nullptr;
+  st = cudaStreamEndCapture(e->stream, &graph);
+  if (s != RBF_OK || st != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return s != RBF_OK ? s : cuda_fail(e, st);
+  }
+  cudaGraphExec_t exec = nullptr;
+  st = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (st != cudaSuccess) return cuda_fail(e, st);
+  e->host_graph[k] = exec;
+  e->host_graph_lists[k] = e->last_lists;
+  return RBF_OK;
+}
+
 rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t* out_idx, float* out_score) {
   if (!e || !query || !out_idx || !out_score) return RBF_ERR_INVALID_VALUE;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
-  const size_t qbytes = static_cast<size_t>(e->d) * 4;
-  std::memcpy(e->h_query, query, qbytes);
-  RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
-  if (rbf_status s = enqueue_score(e, e->query, k)) return s;
+  std::memcpy(e->h_query, query, static_cast<size_t>(e->d) * 4);
   const ResultLayout L = result_layout(static_cast<size_t>(k), 4);
-  if (rbf_status s = enqueue_merge(e, k, e->last_lists, 1, 0, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
-                                   e->d_hres + L.b_off, reinterpret_cast<int*>(e->d_hres)))
-    return s;
+  if (!e->host_graph[k]) {
+    if (rbf_status s = capture_host_search(e, k, L)) return s;
+  } else {
+    // One replay stands for the call's copy and its launches.
+    if (inject(e, 1) || inject(e, 2)) return RBF_ERR_CUDA;
+    e->last_lists = e->host_graph_lists[k];
+    e->last_k = k;
+  }
+  const cudaError_t st = cudaGraphLaunch(e->host_graph[k], e->stream);
+  if (st != cudaSuccess) return cuda_fail(e, st);
   if (rbf_status s = finish_host_call(e, L)) return s;
   std::memcpy(out_idx, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
   std::memcpy(out_score, e->h_result + L.b_off, 4 * static_cast<size_t>(k));
