@@ -178,11 +178,12 @@ rbf_status merge_partial_topk_dev(rbf_engine* engine, int32_t k, int32_t* d_idx,
  * accumulated in fp32.
  *   queries    host, B x D floats
  *   b          1 .. max_batch
- *   k          1 .. min(max_k, N, 32)
+ *   k          1 .. min(max_k, N). Up to 32 each epilogue thread keeps its
+ *              list in registers; above 32 (at most 256) in the engine's
+ *              preallocated partials buffer, 256 queries at a time.
  *   out_idx    host, B x K int32 (row q holds query q's list, best-first)
  *   out_score  host, B x K fp32
- * Errors: INVALID_VALUE, NOT_READY, UNSUPPORTED (k > 32: the fused select
- * keeps 32 keys per query and CTA), CUDA, TIMEOUT. */
+ * Errors: INVALID_VALUE, NOT_READY, CUDA, TIMEOUT. */
 rbf_status search_resident_batch(rbf_engine* engine, const float* queries, int32_t b, int32_t k,
                                  int32_t* out_idx, float* out_score);
 

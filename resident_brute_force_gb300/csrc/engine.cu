@@ -60,6 +60,7 @@ struct rbf_engine {
   void* query_bf16 = nullptr;    // query_rows x max_pitch_bf16
   float* query_f32 = nullptr;    // tf32 batched path (no bf16 copy): query_rows x max_pitch floats
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
+  int* lens = nullptr;           // batched K > 32: keys in each per-CTA list of a 256-query group
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
@@ -259,6 +260,7 @@ void release(rbf_engine* e) {
   cudaFree(e->query_bf16);
   cudaFree(e->query_f32);
   cudaFree(e->theta0);
+  cudaFree(e->lens);
   cudaFree(e->query);
   cudaFree(e->partials);
   cudaFree(e->errw);
@@ -332,6 +334,9 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   e->query_rows = static_cast<int>(align_up(static_cast<size_t>(max_batch), kBatchQueriesPerLaunch));
   const size_t batch_keys = static_cast<size_t>(max_batch) * e->num_sms * kBatchListWidth;
   e->partials_cap = std::max(e->partials_cap, batch_keys);
+  // K > 32: one group of 256 queries at a time, lists of list_width(K) keys.
+  if (max_k > kBatchRegMaxK)
+    e->partials_cap = std::max(e->partials_cap, static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms * kpmax);
   if (flags & RBF_FLAG_BF16_CORPUS) {
     flags |= RBF_FLAG_FP32_CORPUS;  // uploads are converted from the fp32 copy
     e->flags = flags;
@@ -351,6 +356,8 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
     ok = ok && cudaMalloc(&e->query_f32, static_cast<size_t>(e->query_rows) * e->max_pitch * 4) == cudaSuccess;
   }
   ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->lens, static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms * sizeof(int)) ==
+                 cudaSuccess;
   ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
@@ -561,7 +568,6 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
 // epilogue select once per group of up to 256 queries, merge every query.
 static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, int k, int32_t* d_idx, float* d_score,
                                 int* result_err) {
-  if (k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
   if (!e->tmaps_ready) return RBF_ERR_NOT_READY;
   const int64_t rows_total = static_cast<int64_t>(align_up(static_cast<size_t>(b), 128));
   const bool tf32 = e->corpus_bf16 == nullptr;
@@ -605,15 +611,20 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     *lists = grid;
     return RBF_OK;
   };
-  // Pre-pass over the first kSampleRows rows (one 128-row tile per CTA):
-  // no selection, each CTA keeps per query the best key of every 32-row
-  // chunk, and the merge takes the K-th largest of those 512 chunk maxima.
-  // K distinct rows score at least that much, so it is a lower bound on the
-  // final K-th key, and the main pass drops every key below it.
+  // Pre-pass over the first S rows: no selection, each CTA keeps per query
+  // the best key of each of 4 chunks of the rows it scores, and the merge
+  // takes the K-th largest of those chunk maxima (4 per CTA, 512 at S =
+  // 16,384). K distinct rows score at least that much, so it is a lower
+  // bound on the final K-th key, and the main pass drops every key below it.
+  // About K * N / S keys pass it; above K = 32 each one costs a merge into a
+  // list in global memory, so S grows with K (16,384 per 32 of K), up to a
+  // quarter of the corpus.
   const uint64_t* theta0 = nullptr;
-  if (e->n >= 4 * kSampleRows && kSampleRows / 128 <= e->num_sms) {
+  const int64_t sample_rows =
+      std::min<int64_t>(kSampleRows * ((k + 31) / 32), e->n / 4 / kSampleRows * kSampleRows);
+  if (sample_rows >= kSampleRows) {
     int lists = 0;
-    if (rbf_status st = score_groups(kSampleRows, 1, nullptr, &lists)) return st;
+    if (rbf_status st = score_groups(sample_rows, 1, nullptr, &lists)) return st;
     MergeLaunch m;
     m.partials = e->partials;
     m.lists = lists;
@@ -626,12 +637,59 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     m.err_sticky = nullptr;
     m.result_err = nullptr;
     m.kth_out = e->theta0;
+    m.stride = kBatchListWidth;
     RBF_LAUNCH(e, launch_merge(m, e->stream));
     theta0 = e->theta0;
   }
-  int grid = 0;
-  if (rbf_status st = score_groups(e->n, 0, theta0, &grid)) return st;
-  return enqueue_merge(e, k, grid, b, 0, d_idx, d_score, result_err);
+  if (k <= kBatchRegMaxK) {
+    int grid = 0;
+    if (rbf_status st = score_groups(e->n, 0, theta0, &grid)) return st;
+    return enqueue_merge(e, k, grid, b, 0, d_idx, d_score, result_err);
+  }
+  // K > 32: each group of 256 queries is scored (CTA pairs, each thread's
+  // list in the partials buffer with its length in `lens`) and merged before
+  // the next group reuses the buffer. The last merge hands the call's error
+  // word over.
+  const int64_t pair_tiles = (e->n + 255) / 256;
+  const int grid = 2 * static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pair_tiles, e->num_sms / 2)));
+  const int kw = list_width(k);
+  if (static_cast<size_t>(kBatchQueriesPerLaunch) * grid * kw > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+  for (int q0 = 0; q0 < b; q0 += kBatchQueriesPerLaunch) {
+    const int qc = std::min(kBatchQueriesPerLaunch, b - q0);
+    const bool last = q0 + qc == b;
+    GemmSelectLaunch a;
+    a.tmap_q = &e->tmap_query;
+    a.tmap_c = &e->tmap_corpus;
+    a.partials = e->partials;
+    a.err = e->errw;
+    a.n = e->n;
+    a.kchunks = tf32 ? (e->d + 31) / 32 : e->pitch_bf16 / 64;
+    a.tf32 = tf32 ? 1 : 0;
+    a.q_row0 = q0;
+    a.q_count = qc;
+    a.q_out0 = 0;
+    a.k = k;
+    a.grid = grid;
+    a.timeout_ns = e->timeout_ns;
+    a.theta0 = theta0;
+    a.lens = e->lens;
+    RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+    MergeLaunch m;
+    m.partials = e->partials;
+    m.lists = grid;
+    m.queries = qc;
+    m.k = k;
+    m.int_keys = 0;
+    m.out_a = d_idx + static_cast<size_t>(q0) * k;
+    m.out_b = d_score + static_cast<size_t>(q0) * k;
+    m.err_call = last ? e->errw : nullptr;
+    m.err_sticky = e->errw + 1;
+    m.result_err = last ? result_err : nullptr;
+    m.stride = kw;
+    m.lens = e->lens;
+    RBF_LAUNCH(e, launch_merge(m, e->stream));
+  }
+  return RBF_OK;
 }
 
 rbf_status search_resident_batch_dev(rbf_engine* e, const float* d_queries, int32_t b, int32_t k, int32_t* d_idx,
@@ -647,7 +705,6 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (!e || !queries || !out_idx || !out_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
-  if (k > kBatchMaxK) return RBF_ERR_UNSUPPORTED;
   const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
   std::memcpy(e->h_query, queries, qbytes);
   RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));

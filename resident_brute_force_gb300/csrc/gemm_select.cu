@@ -177,14 +177,15 @@ struct Operand {
 
 // ------------------------------------------------- per-thread key lists
 
-// Descending bitonic sort of 8 keys in registers.
-__device__ __forceinline__ void sort8_desc(uint64_t (&c)[8]) {
+// Descending bitonic sort of N (a power of two) keys in registers.
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t (&c)[N]) {
 #pragma unroll
-  for (int k = 2; k <= 8; k <<= 1) {
+  for (int k = 2; k <= N; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < N; ++i) {
         const int l = i ^ j;
         if (l > i) {
           const uint64_t a = c[i], b = c[l];
@@ -243,7 +244,7 @@ __device__ __forceinline__ float pick(const float (&sc)[32], int j) {
 }
 
 struct Params {
-  uint64_t* partials;  // [queries in batch][grid][32] keys
+  uint64_t* partials;  // [queries][grid][32] keys; K > 32: [queries][grid][KP], lens[queries][grid] long
   int* err;
   int64_t n;           // corpus rows
   int num_tiles;       // ceil(n / 128)
@@ -256,6 +257,7 @@ struct Params {
   uint64_t timeout_ns;
   const uint64_t* theta0;  // optional per-query lower bound on the K-th key
   int bound_mode;          // 1: write the best key of each 32-row chunk instead of a top-K list
+  int* lens;               // K > 32: valid keys of each list
 };
 
 template <int KP, bool TF32>
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // make the top K, so theta starts at b - 1.
     uint64_t floor_key = 0;
     if (p.theta0 && qlocal < p.q_count) {
-      const uint64_t b0 = p.theta0[p.q_out0 + qlocal];
+      const uint64_t b0 = p.theta0[p.q_row0 + qlocal];
       floor_key = b0 > 0 ? b0 - 1 : 0;
     }
     uint64_t theta = floor_key;
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t c[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] = (b8 + i < cnt) ? cand[(b8 + i) * 256 + slot] : 0ull;
-        sort8_desc(c);
+        sort_desc(c);
         list_merge8<KP>(L, c);
       }
       cnt = 0;
@@ -436,10 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (m < p.num_mt && p.bound_mode) {
-      // Bound mode: per query, the best key of each 32-row chunk. Any K of
-      // these belong to K distinct rows, so the K-th largest of them over all
-      // CTAs is a lower bound on the query's K-th key. At most 4 per tile are
-      // kept (one CTA scores one tile here); they are written best first.
+      // Bound mode: per query, the best key of each of 4 chunks (chunk c:
+      // rows 32c..32c+31 of every tile the CTA scores). Any K of these belong
+      // to K distinct rows, so the K-th largest of them over all CTAs is a
+      // lower bound on the query's K-th key. They are written best first.
       uint64_t best[4] = {0ull, 0ull, 0ull, 0ull};
       int tile_i = 0;
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
@@ -805,12 +807,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slot = h * 128 + qlocal;                        // candidate buffer column
     const uint32_t acc_empty_leader0 = cluster_addr(&acc_empty[0], 0);
     const uint32_t acc_empty_leader1 = cluster_addr(&acc_empty[1], 0);
-    uint64_t L[KP];
+    // K <= 32: the thread's best-first list of KP keys is in registers.
+    // K > 32 (KP = 64, 128 or 256): it is the thread's own partials list in
+    // global memory, `len` keys long, and buffered candidates are merged into
+    // it from the back; on random data with the sample bound only a few dozen
+    // keys per thread ever reach it.
+    constexpr bool kWide = KP > 32;
+    uint64_t L[kWide ? 1 : KP];
 #pragma unroll
-    for (int i = 0; i < KP; ++i) L[i] = 0;
+    for (int i = 0; i < (kWide ? 1 : KP); ++i) L[i] = 0;
+    const bool live = qidx < p.q_count;
+    auto list_id = [&]() {
+      return static_cast<size_t>(p.q_out0 + qidx) * gridDim.x + static_cast<size_t>(cluster * 2 + h);
+    };
+    uint64_t* lst = nullptr;
+    if constexpr (kWide) lst = p.partials + list_id() * KP;
+    int len = 0;
     uint64_t floor_key = 0;
-    if (p.theta0 && qidx < p.q_count) {
-      const uint64_t b0 = p.theta0[p.q_out0 + qidx];
+    if (p.theta0 && live) {
+      const uint64_t b0 = p.theta0[p.q_row0 + qidx];
       floor_key = b0 > 0 ? b0 - 1 : 0;
     }
     uint64_t theta = floor_key;
@@ -819,19 +834,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cnt = 0;
 
     auto merge_buffer = [&]() {
-      const int batches = static_cast<int>((__reduce_max_sync(kFullMask, static_cast<unsigned>(cnt)) + 7u) >> 3);
-#pragma unroll 1
-      for (int b8 = 0; b8 < batches * 8; b8 += 8) {
-        uint64_t c[8];
+      if constexpr (kWide) {
+        if (cnt > 0) {
+          uint64_t c[kCandCap];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = (b8 + i < cnt) ? cand[(b8 + i) * 256 + slot] : 0ull;
-        sort8_desc(c);
-        list_merge8<KP>(L, c);
+          for (int i = 0; i < kCandCap; ++i) c[i] = i < cnt ? cand[i * 256 + slot] : 0ull;
+          sort_desc(c);
+          // Merge into the list without a chain of dependent loads: list
+          // key x moves up by s(x) = the number of candidates above it, and
+          // candidate j lands at j + the number of list keys above it.
+          // Keys are read back to front, kScan independent loads at a time,
+          // and moved (at most K kept); the scan stops at the first batch
+          // that reaches a key no candidate beats (it and everything before
+          // it stay). above[j / 2] counts, in its low or high 16 bits, the
+          // scanned keys above candidate j.
+          constexpr int kScan = 4;
+          uint32_t above[kCandCap / 2];
+#pragma unroll
+          for (int j = 0; j < kCandCap / 2; ++j) above[j] = 0;
+          int i = len;
+#pragma unroll 1
+          while (i > 0) {
+            const int i0 = i > kScan ? i - kScan : 0;
+            uint64_t x[kScan];
+#pragma unroll
+            for (int u = 0; u < kScan; ++u) x[u] = i0 + u < i ? lst[i0 + u] : ~0ull;
+            bool reached = false;
+#pragma unroll
+            for (int u = kScan - 1; u >= 0; --u) {
+              int sh = 0;
+#pragma unroll
+              for (int j = 0; j < kCandCap; ++j) sh += c[j] > x[u] ? 1 : 0;
+              const bool valid = i0 + u < i;
+              reached |= valid && sh == 0;
+              if (valid && sh > 0 && i0 + u + sh < p.k) lst[i0 + u + sh] = x[u];
+#pragma unroll
+              for (int j = 0; j < kCandCap; ++j)
+                above[j / 2] += (valid && sh <= j) ? (1u << (16 * (j & 1))) : 0u;
+            }
+            i = i0;
+            if (reached) break;
+          }
+#pragma unroll
+          for (int j = 0; j < kCandCap; ++j) {
+            const int at = j + i + static_cast<int>((above[j / 2] >> (16 * (j & 1))) & 0xFFFFu);
+            if (j < cnt && at < p.k) lst[at] = c[j];
+          }
+          len = min(len + cnt, p.k);
+          cnt = 0;
+          if (len == p.k) {
+            theta = umax64(lst[p.k - 1], floor_key);
+            filling = theta == 0;
+            theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
+          }
+        }
+      } else {
+        const int batches = static_cast<int>((__reduce_max_sync(kFullMask, static_cast<unsigned>(cnt)) + 7u) >> 3);
+#pragma unroll 1
+        for (int b8 = 0; b8 < batches * 8; b8 += 8) {
+          uint64_t c[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) c[i] = (b8 + i < cnt) ? cand[(b8 + i) * 256 + slot] : 0ull;
+          sort_desc(c);
+          list_merge8<KP>(L, c);
+        }
+        cnt = 0;
+        theta = umax64(list_get<KP>(L, p.k - 1), floor_key);
+        filling = theta == 0;
+        theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
       }
-      cnt = 0;
-      theta = umax64(list_get<KP>(L, p.k - 1), floor_key);
-      filling = theta == 0;
-      theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
     };
 
     int tile_i = 0;
@@ -867,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
           if (filling) m = 0xFFFFFFFFu;
           if (p.n - rb < 32) m &= (p.n - rb > 0) ? ((1u << (p.n - rb)) - 1u) : 0u;
+          if (!live) m = 0;
           uint32_t u = __reduce_or_sync(kFullMask, m);
           while (u) {
             const int j = __ffs(u) - 1;
@@ -884,13 +956,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
-    if (qidx < p.q_count) {
-      uint64_t* dst =
-          p.partials + (static_cast<size_t>(p.q_out0 + qidx) * gridDim.x + static_cast<size_t>(cluster * 2 + h)) * 32;
+    if (live) {
+      if constexpr (kWide) {
+        p.lens[list_id()] = len;
+      } else {
+        uint64_t* dst = p.partials + list_id() * 32;
 #pragma unroll
-      for (int i = 0; i < KP; ++i) dst[i] = L[i];
+        for (int i = 0; i < KP; ++i) dst[i] = L[i];
 #pragma unroll
-      for (int i = KP; i < 32; ++i) dst[i] = 0ull;
+        for (int i = KP; i < 32; ++i) dst[i] = 0ull;
+      }
     }
   }
 
@@ -1067,12 +1142,17 @@ cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64
 template <bool TF32>
 cudaError_t launch_typed(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, const GemmSelectLaunch& a,
                          cudaStream_t stream) {
-  if (a.bound_mode) {
-    // Bound mode writes 4 keys per tile and query: one tile per CTA.
-    if (p.num_tiles > a.grid) return cudaErrorInvalidValue;
-    return launch_t<8, TF32>(tq, tc, p, a.grid, stream);
-  }
+  if (a.bound_mode) return launch_t<8, TF32>(tq, tc, p, a.grid, stream);
   if (a.grid < 2 || a.grid % 2 != 0) return cudaErrorInvalidValue;
+  if (a.k > 32) {
+    // Lists in global memory, any number of queries: CTA pairs.
+    if (!a.lens) return cudaErrorInvalidValue;
+    // List stride list_width(K), as the merge reads it.
+    if (a.k <= 64) return launch_pair_t<64, TF32>(tq, tc, p, a.grid, stream);
+    if (a.k <= 128) return launch_pair_t<128, TF32>(tq, tc, p, a.grid, stream);
+    if (a.k <= 256) return launch_pair_t<256, TF32>(tq, tc, p, a.grid, stream);
+    return cudaErrorInvalidValue;
+  }
   if (a.q_count > 128) {
     // Two M tiles: a CTA pair per 256-row tile (lists per query = grid).
     if (a.k <= 8) return launch_pair_t<8, TF32>(tq, tc, p, a.grid, stream);
@@ -1101,6 +1181,7 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.timeout_ns = a.timeout_ns;
   p.theta0 = a.theta0;
   p.bound_mode = a.bound_mode;
+  p.lens = a.lens;
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
   return a.tf32 ? launch_typed<true>(tq, tc, p, a, stream) : launch_typed<false>(tq, tc, p, a, stream);

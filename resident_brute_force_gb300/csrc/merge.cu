@@ -31,6 +31,8 @@ struct Params {
   int* result_err;
   uint64_t* kth_out;  // optional: the K-th key of each query
   int smem_bytes;     // dynamic shared memory of the launch
+  int stride;         // keys from one list to the next
+  const int* lens;    // optional: [query][list] valid keys per list
 };
 
 constexpr int kManyQueries = 64;          // from this many queries on, merge CTAs are 8 warps
@@ -41,7 +43,7 @@ template <int KP, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Params p) {
   extern __shared__ __align__(16) uint64_t smem[];
   pdl_wait();
-  const uint64_t* base = p.partials + static_cast<size_t>(blockIdx.x) * p.lists * KP;
+  const uint64_t* base = p.partials + static_cast<size_t>(blockIdx.x) * p.lists * p.stride;
   MergeOut o;
   o.k = p.k;
   o.int_keys = p.int_keys;
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
   o.out_b = p.out_b;
   o.kth_out = p.kth_out;
   o.q = blockIdx.x;
+  o.stride = p.stride;
+  o.lens = p.lens ? p.lens + static_cast<size_t>(blockIdx.x) * p.lists : nullptr;
   mergecore::merge_lists<KP, WARPS * 32>(o, base, p.lists, smem, p.smem_bytes, kStageKeys);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.err_call) {
     // Hand the per-call device error word to the host-visible result and
@@ -100,6 +104,8 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
   p.kth_out = a.kth_out;
+  p.stride = a.stride > 0 ? a.stride : list_width(a.k);
+  p.lens = a.lens;
   // One query: a wide CTA to shorten the single merge. Many queries: 8-warp
   // CTAs, so that several fit on each SM and all queries run in one wave.
   if (a.queries >= kManyQueries) {

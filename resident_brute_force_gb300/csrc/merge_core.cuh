@@ -35,7 +35,9 @@ namespace mergecore {
 
 // Where one query's result goes: K entries at q*K of out_a / out_b (int32
 // value + int64 position for integer keys, int32 index + fp32 score for score
-// keys), and optionally the K-th key at kth_out[q].
+// keys), and optionally the K-th key at kth_out[q]. The lists are `stride`
+// keys apart; with `lens` list l holds lens[l] keys (entries past that are
+// never read and count as empty), else all `stride`.
 struct MergeOut {
   int k;
   int int_keys;
@@ -43,7 +45,17 @@ struct MergeOut {
   void* out_b;
   uint64_t* kth_out;
   size_t q;
+  int stride;
+  const int* lens;
 };
+
+// Valid keys of list l.
+__device__ __forceinline__ int list_len(const MergeOut& p, int l) { return p.lens ? p.lens[l] : p.stride; }
+
+// Key e of list l, or the empty key past the list's end.
+__device__ __forceinline__ uint64_t list_key(const MergeOut& p, const uint64_t* base, int l, int e) {
+  return e < list_len(p, l) ? __ldcg(base + static_cast<size_t>(l) * p.stride + e) : 0ull;
+}
 
 constexpr int kSurvivorCap = 2048;  // keys gathered by the fast path
 constexpr int kFastMaxLists = 512;  // lists the bound selection handles (its work grows as lists^2)
@@ -61,11 +73,13 @@ __device__ __forceinline__ void emit(const MergeOut& p, int e, uint64_t key) {
 }
 
 // Copy the first k keys of lists [l0, l0 + count) to dst (list-major, k per
-// list) with U loads in flight per thread before any is stored, so the copy
-// costs one L2 round trip per U x threads keys (16 for CTAs of up to 256
-// threads, 8 for wider ones, which must stay within 64 registers).
-template <int KP, int NT, int U = (NT <= 256 ? 16 : 8)>
-__device__ __forceinline__ void stage_heads(uint64_t* dst, const uint64_t* base, int l0, int count, int k) {
+// list, empty keys past a list's end) with U loads in flight per thread
+// before any is stored, so the copy costs one L2 round trip per U x threads
+// keys (16 for CTAs of up to 256 threads, 8 for wider ones, which must stay
+// within 64 registers).
+template <int NT, int U = (NT <= 256 ? 16 : 8)>
+__device__ __forceinline__ void stage_heads(const MergeOut& p, uint64_t* dst, const uint64_t* base, int l0, int count,
+                                            int k) {
   const int total = count * k;
   for (int i0 = 0; i0 < total; i0 += U * NT) {
     uint64_t r[U];
@@ -75,7 +89,7 @@ __device__ __forceinline__ void stage_heads(uint64_t* dst, const uint64_t* base,
       r[u] = 0;
       if (i < total) {
         const int l = i / k;
-        r[u] = __ldcg(base + static_cast<size_t>(l0 + l) * KP + (i - l * k));
+        r[u] = list_key(p, base, l0 + l, i - l * k);
       }
     }
 #pragma unroll
@@ -127,7 +141,7 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
     s_bound = 1;  // excludes the empty slots (key 0)
     s_count = 0;
   }
-  stage_heads<KP, NT>(stage, base, 0, L, P);
+  stage_heads<NT>(p, stage, base, 0, L, P);
   __syncthreads();
   uint64_t* row = surv;  // the lists' t-th keys, contiguous (the survivors come later)
   for (int l = tid; l < L; l += NT) row[l] = stage[l * P + t - 1];
@@ -147,7 +161,7 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
     greater += __shfl_xor_sync(kFullMask, greater, 2);
     greater += __shfl_xor_sync(kFullMask, greater, 4);
     if (l < L && part == 0) {
-      uint64_t b = k <= P ? stage[l * P + k - 1] : __ldcg(base + static_cast<size_t>(l) * KP + k - 1);
+      uint64_t b = k <= P ? stage[l * P + k - 1] : list_key(p, base, l, k - 1);
       if (greater == m - 1) b = umax64(b, x);
       atomicMax(&s_bound, static_cast<unsigned long long>(b));
     }
@@ -162,7 +176,7 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
     for (int e0 = 0; e0 < k; e0 += 32) {
       const int e = e0 + lane;
       uint64_t key = 0;
-      if (e < k) key = e < P ? stage[l * P + e] : __ldcg(base + static_cast<size_t>(l) * KP + e);
+      if (e < k) key = e < P ? stage[l * P + e] : list_key(p, base, l, e);
       const bool pass = key >= bound;
       const unsigned msk = __ballot_sync(kFullMask, pass);
       if (msk == 0) break;
@@ -197,7 +211,7 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
 
 
 // The general merge: lists staged stage_lists at a time after WARPS lists of
-// KP keys used as the tree; each warp folds a strided subset of the staged
+// KP >= K keys used as the tree; each warp folds a strided subset of the staged
 // lists into its register list, then the warp lists merge pairwise.
 template <int KP, int NT>
 __device__ void merge_general(const MergeOut& p, const uint64_t* base, int L, uint64_t* smem, int stage_lists) {
@@ -211,7 +225,7 @@ __device__ void merge_general(const MergeOut& p, const uint64_t* base, int L, ui
   warp_list_clear<R>(v);
   for (int g0 = 0; g0 < L; g0 += stage_lists) {
     const int gl = min(stage_lists, L - g0);
-    stage_heads<KP, NT>(stage, base, g0, gl, p.k);
+    stage_heads<NT>(p, stage, base, g0, gl, p.k);
     __syncthreads();
     for (int l = warp; l < gl; l += WARPS) {
       const uint64_t* src = stage + l * p.k;
@@ -243,10 +257,10 @@ __device__ void merge_general(const MergeOut& p, const uint64_t* base, int L, ui
   }
 }
 
-// One query's merge by all NT threads of the CTA over L lists of KP keys at
-// base, in smem_bytes of dynamic shared memory (at least
-// fast_smem_bytes(L, k, stage_keys) or, for the general merge, room for
-// NT/32 lists of KP keys and one staged list). Block-uniform; ends with the
+// One query's merge by all NT threads of the CTA over the L lists at base
+// (KP >= K: the register list width of the general merge), in smem_bytes of
+// dynamic shared memory (at least fast_smem_bytes(L, k, stage_keys) or, for
+// the general merge, room for NT/32 lists of KP keys and one staged list). Block-uniform; ends with the
 // outputs written (no barrier after the last write).
 template <int KP, int NT>
 __device__ void merge_lists(const MergeOut& p, const uint64_t* base, int L, uint64_t* smem, int smem_bytes,

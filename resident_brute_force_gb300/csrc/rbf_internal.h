@@ -43,7 +43,7 @@ int score_select_smem_bytes(int pitch, int k, int rows_per_stage, int stages);
 cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream);
 
 struct MergeLaunch {
-  const uint64_t* partials;  // device, queries x lists x list_width(k) keys
+  const uint64_t* partials;  // device, queries x lists x stride keys
   int lists;                 // lists per query
   int queries;               // one CTA per query
   int k;
@@ -54,6 +54,8 @@ struct MergeLaunch {
   int* err_sticky;           // sticky error word (ORed)
   int* result_err;           // where the per-call error lands (may be null)
   uint64_t* kth_out = nullptr;  // optional: each query's K-th key
+  int stride = 0;               // keys from one list to the next (0: list_width(k))
+  const int* lens = nullptr;    // optional [queries x lists] valid keys per list (else all stride)
 };
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
 
@@ -100,7 +102,7 @@ cudaError_t launch_normalize_queries_bf16(const float* src, int64_t src_pitch, v
 
 // Batched queries (tensor cores). K <= 32; each launch covers up to 256
 // queries; every CTA writes 32 keys per query.
-constexpr int kBatchMaxK = 32;
+constexpr int kBatchRegMaxK = 32;  // batched K up to this: per-thread lists in registers
 constexpr int kBatchQueriesPerLaunch = 256;
 constexpr int kBatchListWidth = 32;
 constexpr int kBf16PitchAlign = 64;  // bf16 elements: one 128-byte swizzle row
@@ -108,7 +110,7 @@ constexpr int kBf16PitchAlign = 64;  // bf16 elements: one 128-byte swizzle row
 struct GemmSelectLaunch {
   const void* tmap_q;        // host CUtensorMap over the bf16 query buffer
   const void* tmap_c;        // host CUtensorMap over the bf16 corpus
-  uint64_t* partials;        // [queries][grid][32] keys
+  uint64_t* partials;        // [queries][grid][32] keys; K > 32: [queries][grid][list_width(K)]
   int* err;
   int64_t n;                 // corpus rows
   int kchunks;               // 128-byte K chunks per row (64 bf16 or 32 fp32 elements each)
@@ -120,8 +122,10 @@ struct GemmSelectLaunch {
   int grid;                  // even: 2 x min(ceil(n / 256), SMs / 2); also the lists per query
   uint64_t timeout_ns;
   const uint64_t* theta0;    // optional per-query lower bound on the K-th key (keys >= it are kept)
-  int bound_mode = 0;        // 1: no selection; each CTA writes, per query, the best key of every
-                             // 32-row chunk it scored (at most 4 per tile, best first, then zeros)
+  int bound_mode = 0;        // 1: no selection; each CTA writes, per query, the best key of each of 4
+                             // chunks of its rows (chunk c: rows 32c..32c+31 of each of its tiles),
+                             // best first, then zeros
+  int* lens = nullptr;       // K > 32: [queries][grid] valid keys of each list (required)
 };
 int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.

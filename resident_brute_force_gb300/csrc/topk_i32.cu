@@ -455,6 +455,8 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     o.out_b = p.out_pos;
     o.kth_out = nullptr;
     o.q = 0;
+    o.stride = KP;
+    o.lens = nullptr;
     mergecore::merge_lists<KP, kSThreads>(o, p.partials, static_cast<int>(gridDim.x),
                                           reinterpret_cast<uint64_t*>(smem), kMergeSmemBytes, kMergeStageKeys);
     if (threadIdx.x == 0) {

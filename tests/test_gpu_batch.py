@@ -91,14 +91,17 @@ def test_dev_matches_host_and_repeats(rbf):
         assert e.check_device_error() == rbf.RBF_OK
 
 
-def test_unsupported_and_invalid(rbf):
+def test_invalid_and_k_above_32(rbf):
     c = workloads.dyadic_grid(500, 64, seed=21)
     qs = workloads.dyadic_grid(4, 64, seed=22)
     with engine(rbf, 500, 64, 4, k=64) as e:
         e.upload_corpus_rowmajor(c)
+        idx, sc = e.search_resident_batch(qs, 33)       # lists in global memory from K = 33 on
+        for j in range(4):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], 33))
         with pytest.raises(rbf.RbfError) as ei:
-            e.search_resident_batch(qs, 33)             # the fused select keeps K <= 32
-        assert ei.value.status == rbf.RBF_ERR_UNSUPPORTED
+            e.search_resident_batch(qs, 65)
+        assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
         with pytest.raises(rbf.RbfError) as ei:
             e.search_resident_batch(np.concatenate([qs, qs]), 8)
         assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
