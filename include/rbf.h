@@ -76,7 +76,11 @@ typedef enum rbf_option {
   RBF_OPT_STAGE_BYTES = 2,   /* target bytes per pipeline stage (default 65536) */
   RBF_OPT_SMEM_BUDGET = 3,   /* shared-memory ring budget per CTA, bytes */
   RBF_OPT_TIMEOUT_NS = 4,    /* bound on every device-side wait (default 2e9) */
-  RBF_OPT_SCHEDULE = 5       /* 0 = static row ranges, 1 = dynamic tile claims (default) */
+  RBF_OPT_SCHEDULE = 5,      /* 0 = static row ranges, 1 = dynamic tile claims (default) */
+  RBF_OPT_BATCH_SAMPLE = 6   /* rows of the batched path's bound pre-pass: -1 = automatic
+                                (default: 16,384 per 32 of K, at most N/4, none below 16,384),
+                                0 = no pre-pass, else that many leading rows (a multiple of 256,
+                                at most N). Changes speed only, never results. */
 } rbf_option;
 
 /* ------------------------------------------------------------------ engine */

@@ -61,6 +61,7 @@ struct rbf_engine {
   float* query_f32 = nullptr;    // tf32 batched path (no bf16 copy): query_rows x max_pitch floats
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
   int* lens = nullptr;           // batched K > 32: keys in each per-CTA list of a 256-query group
+  int64_t batch_sample = -1;     // RBF_OPT_BATCH_SAMPLE
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
@@ -427,6 +428,10 @@ rbf_status rbf_set_option(rbf_engine* e, rbf_option opt, int64_t value) {
       if (value != 0 && value != 1) return RBF_ERR_INVALID_VALUE;
       e->dynamic = static_cast<int>(value);
       return RBF_OK;
+    case RBF_OPT_BATCH_SAMPLE:
+      if (value < -1 || (value > 0 && value % 256 != 0)) return RBF_ERR_INVALID_VALUE;
+      e->batch_sample = value;
+      return RBF_OK;
   }
   return RBF_ERR_INVALID_VALUE;
 }
@@ -606,23 +611,29 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
       a.timeout_ns = e->timeout_ns;
       a.theta0 = theta0;
       a.bound_mode = bound_mode;
+      // Only the first launch after the query staging waits for it before
+      // streaming (after the bound merge, or another group, the queries are
+      // long complete).
+      a.wait_inputs = (q0 == 0 && (bound_mode || theta0 == nullptr)) ? 1 : 0;
       RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
     }
     *lists = grid;
     return RBF_OK;
   };
-  // Pre-pass over the first S rows: no selection, each CTA keeps per query
-  // the best key of each of 4 chunks of the rows it scores, and the merge
-  // takes the K-th largest of those chunk maxima (4 per CTA, 512 at S =
-  // 16,384). K distinct rows score at least that much, so it is a lower
+  // Pre-pass over the first S rows: no selection, each per-CTA list of a
+  // query holds the best key of each of 4 chunks of the rows it covers, and
+  // the merge takes the K-th largest of those chunk maxima (4 per list, 512
+  // at S = 16,384). K distinct rows score at least that much, so it is a lower
   // bound on the final K-th key, and the main pass drops every key below it.
   // About K * N / S keys pass it; above K = 32 each one costs a merge into a
   // list in global memory, so S grows with K (16,384 per 32 of K), up to a
   // quarter of the corpus.
   const uint64_t* theta0 = nullptr;
   const int64_t sample_rows =
-      std::min<int64_t>(kSampleRows * ((k + 31) / 32), e->n / 4 / kSampleRows * kSampleRows);
-  if (sample_rows >= kSampleRows) {
+      e->batch_sample < 0
+          ? std::min<int64_t>(kSampleRows * ((k + 31) / 32), e->n / 4 / kSampleRows * kSampleRows)
+          : std::min<int64_t>(e->batch_sample, e->n);
+  if (sample_rows >= 256) {
     int lists = 0;
     if (rbf_status st = score_groups(sample_rows, 1, nullptr, &lists)) return st;
     MergeLaunch m;
@@ -638,6 +649,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     m.result_err = nullptr;
     m.kth_out = e->theta0;
     m.stride = kBatchListWidth;
+    m.short_lists = k > kBatchRegMaxK ? 1 : 0;  // 4 chunk maxima per list
     RBF_LAUNCH(e, launch_merge(m, e->stream));
     theta0 = e->theta0;
   }
@@ -673,6 +685,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     a.timeout_ns = e->timeout_ns;
     a.theta0 = theta0;
     a.lens = e->lens;
+    a.wait_inputs = (q0 == 0 && theta0 == nullptr) ? 1 : 0;
     RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
     MergeLaunch m;
     m.partials = e->partials;
@@ -687,6 +700,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     m.result_err = last ? result_err : nullptr;
     m.stride = kw;
     m.lens = e->lens;
+    m.short_lists = 1;
     RBF_LAUNCH(e, launch_merge(m, e->stream));
   }
   return RBF_OK;

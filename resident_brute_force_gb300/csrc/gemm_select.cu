@@ -8,21 +8,31 @@
 // 3-4: per-block partial top-K, then a merge): every CTA leaves one
 // best-first list per query, and the merge kernel finishes each query.
 //
-// One CTA per SM, 10 warps:
-//   warp 0     TMA producer: per 64-wide K chunk, the query tile(s) (up to
-//              256 queries = two 128-row M tiles) and 128 corpus rows, 128-byte
-//              swizzled, into a 4-stage shared-memory ring. The bf16 corpus is
+// Two kernels, one CTA per SM, 10 warps each:
+//   gemm_select_pair_kernel  129-256 queries, every K > 32 and the bound
+//              pre-pass: clusters of two CTAs, tcgen05.mma.cta_group::2 with
+//              M = 256 queries (128 per CTA) and N = 256 corpus rows (128 per
+//              CTA), 6 stages of 32 KB;
+//   gemm_select_kernel       up to 128 queries with K <= 32: one CTA per
+//              128-row tile, M = 128, N = 128, 4 stages of 48 KB.
+// In both:
+//   warp 0     TMA producer: per 128-byte K chunk (64 bf16 or 32 fp32
+//              elements) the CTA's queries and corpus rows, 128-byte
+//              swizzled, into the shared-memory ring. The bf16 corpus is
 //              stored tile-major ([row tile][K chunk][128 rows][64]), so each
 //              corpus load is one contiguous 16 KB block of HBM;
-//   warp 1     TMEM owner and MMA issuer: one thread issues
-//              tcgen05.mma.cta_group::1.kind::f16 (M = 128 queries, N = 128
-//              corpus rows, K = 16) into one of two accumulator buffers, so the
-//              epilogue drains tile t while tile t + 1 accumulates;
-//   warps 2-9  epilogue: thread = one query (its TMEM lane); it reads its 128
-//              scores 32 at a time (tcgen05.ld 32x32b.x32), keeps the keys that
-//              beat its K-th best in a 16-entry shared-memory buffer, and merges
-//              full buffers into a register bitonic list of KP <= 32 keys.
-// The scores never reach memory: each CTA writes 32 keys per query.
+//   warp 1     TMEM owner and MMA issuer: one thread issues the MMAs into one
+//              of two accumulator buffers, so the epilogue drains tile t
+//              while tile t + 1 accumulates;
+//   warps 2-9  epilogue: thread = one query (its TMEM lane) over 128 of the
+//              tile's columns; it marks the scores that may beat its K-th
+//              best, buffers their keys 16 deep in shared memory and merges
+//              full buffers into its best-first list: KP <= 32 keys in
+//              registers, or for K > 32 a list in global memory (the
+//              thread's slot of the partials buffer) with its length.
+// The scores never reach memory: each thread writes one list per query. In
+// bound mode (the pre-pass over a row sample) it writes instead the best key
+// of each of its four 32-column chunks, folded over its tiles.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -256,8 +266,9 @@ struct Params {
   int k;
   uint64_t timeout_ns;
   const uint64_t* theta0;  // optional per-query lower bound on the K-th key
-  int bound_mode;          // 1: write the best key of each 32-row chunk instead of a top-K list
+  int bound_mode;          // 1 (CTA pairs, KP = 8): write 4 chunk maxima per list instead of a top-K list
   int* lens;               // K > 32: valid keys of each list
+  int wait_inputs;         // 1: the queries come from the kernel launched just before this one
 };
 
 template <int KP, bool TF32>
@@ -302,10 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent: the next kernel may be scheduled
+  // now (it waits for this grid before it reads anything written here),
+  // and this one waits for the previous grid before it reads what that
+  // wrote (the queries, the per-query bounds) or writes the lists.
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
+      if (p.wait_inputs) pdl_wait();
       const uint64_t pol_c = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       const uint32_t bytes = static_cast<uint32_t>((p.num_mt + 1) * kSubTileBytes);
@@ -397,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- epilogue
+    pdl_wait();
     const int e = warp - 2;
     const int m = e >> 2;             // M tile
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
@@ -437,61 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
     };
 
-    if (m < p.num_mt && p.bound_mode) {
-      // Bound mode: per query, the best key of each of 4 chunks (chunk c:
-      // rows 32c..32c+31 of every tile the CTA scores). Any K of these belong
-      // to K distinct rows, so the K-th largest of them over all CTAs is a
-      // lower bound on the query's K-th key. They are written best first.
-      uint64_t best[4] = {0ull, 0ull, 0ull, 0ull};
-      int tile_i = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
-        const int b = tile_i & 1;
-        if (!__all_sync(kFullMask, mbar_wait(&acc_full[b], static_cast<uint32_t>(tile_i >> 1) & 1u, p.timeout_ns))) {
-          if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
-          abort_flag = 1;
-          break;
-        }
-        if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) break;
-        tc_fence_after();
-        const int64_t row0 = static_cast<int64_t>(t) * kTileRows;
-#pragma unroll
-        for (int c = 0; c < kTileRows / 32; ++c) {
-          float sc[32];
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                 static_cast<uint32_t>(b * 256 + m * 128 + c * 32);
-          tmem_ld32(taddr, sc);
-          const int64_t rb = row0 + c * 32;
-          uint64_t top = 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint64_t key = (rb + j < p.n) ? make_key(sc[j], static_cast<uint32_t>(rb + j)) : 0ull;
-            top = umax64(top, key);
-          }
-          best[c] = umax64(best[c], top);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
-      }
-      // Best first: a 4-key sorting network.
-      auto cswap = [](uint64_t& x, uint64_t& y) {
-        const uint64_t hi = umax64(x, y), lo = umin64(x, y);
-        x = hi;
-        y = lo;
-      };
-      cswap(best[0], best[1]);
-      cswap(best[2], best[3]);
-      cswap(best[0], best[2]);
-      cswap(best[1], best[3]);
-      cswap(best[1], best[2]);
-      if (qlocal < p.q_count) {
-        uint64_t* dst = p.partials + (static_cast<size_t>(p.q_out0 + qlocal) * gridDim.x + blockIdx.x) * 32;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = best[i];
-#pragma unroll
-        for (int i = 4; i < 32; ++i) dst[i] = 0ull;
-      }
-    } else if (m < p.num_mt) {
+    if (m < p.num_mt) {
       int tile_i = 0;
       for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
         const int b = tile_i & 1;
@@ -704,10 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch, as in gemm_select_kernel: the corpus
+  // stream starts while the previous kernel finishes unless that kernel
+  // wrote the queries; the epilogue waits for it before it reads the bounds
+  // or writes any list.
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // --------------------------------------------------------- TMA producer
     if (lane == 0) {
+      if (p.wait_inputs) pdl_wait();
       const uint64_t pol_c = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       int64_t it = 0;
@@ -799,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- epilogue
+    pdl_wait();
     const int e = warp - 2;
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
     const int h = e >> 2;             // which 128 of the tile's 256 rows
@@ -832,6 +803,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float theta_f = floor_key ? key_score(floor_key + 1) : 0.0f;
     bool filling = floor_key == 0;
     int cnt = 0;
+    // Bound mode (KP = 8 instance only): the best key of each of the 4
+    // 32-row chunks of the thread's 128 columns, folded over its tiles.
+    uint64_t best[4] = {0ull, 0ull, 0ull, 0ull};
+    const bool bound = KP == 8 && p.bound_mode;
 
     auto merge_buffer = [&]() {
       if constexpr (kWide) {
@@ -933,6 +908,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c2 = 0; c2 < 2; ++c2) {
           const float(&sc)[32] = *reinterpret_cast<const float(*)[32]>(&s64[c2 * 32]);
           const int64_t rb = row0 + hh * 64 + c2 * 32;
+          if constexpr (KP == 8) {
+            if (bound) {
+              uint64_t top = 0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                top = umax64(top, (rb + j < p.n) ? make_key(sc[j], static_cast<uint32_t>(rb + j)) : 0ull);
+              best[hh * 2 + c2] = umax64(best[hh * 2 + c2], top);
+              continue;
+            }
+          }
           uint32_t m = 0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
@@ -955,16 +940,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
-    if (live) {
-      if constexpr (kWide) {
-        p.lens[list_id()] = len;
-      } else {
+    if (bound) {
+      // Best first (a 4-key sorting network), then zeros to the list width.
+      auto cswap = [](uint64_t& x, uint64_t& y) {
+        const uint64_t hi = umax64(x, y), lo = umin64(x, y);
+        x = hi;
+        y = lo;
+      };
+      cswap(best[0], best[1]);
+      cswap(best[2], best[3]);
+      cswap(best[0], best[2]);
+      cswap(best[1], best[3]);
+      cswap(best[1], best[2]);
+      if (live) {
         uint64_t* dst = p.partials + list_id() * 32;
 #pragma unroll
-        for (int i = 0; i < KP; ++i) dst[i] = L[i];
+        for (int i = 0; i < 4; ++i) dst[i] = best[i];
 #pragma unroll
-        for (int i = KP; i < 32; ++i) dst[i] = 0ull;
+        for (int i = 4; i < 32; ++i) dst[i] = 0ull;
+      }
+    } else {
+      if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
+      if (live) {
+        if constexpr (kWide) {
+          p.lens[list_id()] = len;
+        } else {
+          uint64_t* dst = p.partials + list_id() * 32;
+#pragma unroll
+          for (int i = 0; i < KP; ++i) dst[i] = L[i];
+#pragma unroll
+          for (int i = KP; i < 32; ++i) dst[i] = 0ull;
+        }
       }
     }
   }
@@ -1002,8 +1008,17 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params&
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  fn<<<grid, kThreads, smem, st>>>(tq, tc, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, tq, tc, p);
 }
 
 int pair_smem_bytes() {
@@ -1025,13 +1040,15 @@ cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tc, const Pa
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, fn, tq, tc, p);
 }
 
@@ -1142,8 +1159,8 @@ cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64
 template <bool TF32>
 cudaError_t launch_typed(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, const GemmSelectLaunch& a,
                          cudaStream_t stream) {
-  if (a.bound_mode) return launch_t<8, TF32>(tq, tc, p, a.grid, stream);
   if (a.grid < 2 || a.grid % 2 != 0) return cudaErrorInvalidValue;
+  if (a.bound_mode) return launch_pair_t<8, TF32>(tq, tc, p, a.grid, stream);
   if (a.k > 32) {
     // Lists in global memory, any number of queries: CTA pairs.
     if (!a.lens) return cudaErrorInvalidValue;
@@ -1182,6 +1199,7 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.theta0 = a.theta0;
   p.bound_mode = a.bound_mode;
   p.lens = a.lens;
+  p.wait_inputs = a.wait_inputs;
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
   return a.tf32 ? launch_typed<true>(tq, tc, p, a, stream) : launch_typed<false>(tq, tc, p, a, stream);

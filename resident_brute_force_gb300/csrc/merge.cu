@@ -33,15 +33,17 @@ struct Params {
   int smem_bytes;     // dynamic shared memory of the launch
   int stride;         // keys from one list to the next
   const int* lens;    // optional: [query][list] valid keys per list
+  int stage_keys;     // shared-memory budget (keys) for staged list heads
 };
 
 constexpr int kManyQueries = 64;          // from this many queries on, merge CTAs are 8 warps
-constexpr int kStageBytes = 160 * 1024;   // shared memory for staged list heads
+constexpr int kStageBytes = 160 * 1024;   // shared memory for staged list heads (at most)
 constexpr int kStageKeys = kStageBytes / 8;
 
 template <int KP, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Params p) {
   extern __shared__ __align__(16) uint64_t smem[];
+  pdl_launch_dependents();  // a following scoring pass may start streaming; it waits before using our output
   pdl_wait();
   const uint64_t* base = p.partials + static_cast<size_t>(blockIdx.x) * p.lists * p.stride;
   MergeOut o;
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
   o.q = blockIdx.x;
   o.stride = p.stride;
   o.lens = p.lens ? p.lens + static_cast<size_t>(blockIdx.x) * p.lists : nullptr;
-  mergecore::merge_lists<KP, WARPS * 32>(o, base, p.lists, smem, p.smem_bytes, kStageKeys);
+  mergecore::merge_lists<KP, WARPS * 32>(o, base, p.lists, smem, p.smem_bytes, p.stage_keys);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.err_call) {
     // Hand the per-call device error word to the host-visible result and
     // the sticky word, then re-arm it for the next call.
@@ -67,8 +69,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
 template <int KP, int WARPS>
 cudaError_t launch_t(Params p, int queries, cudaStream_t stream) {
   auto fn = merge_partials_kernel<KP, WARPS>;
-  const int stage_lists = std::max(1, std::min(p.lists, kStageKeys / p.k));
-  const int smem = std::max(WARPS * KP * 8 + stage_lists * p.k * 8, fast_smem_bytes(p.lists, p.k, kStageKeys));
+  const int stage_lists = std::max(1, std::min(p.lists, p.stage_keys / p.k));
+  const int smem =
+      std::max(WARPS * KP * 8 + stage_lists * p.k * 8, fast_smem_bytes(p.lists, p.k, p.stage_keys));
   p.smem_bytes = smem;
   static int configured = 0;
   const int want = WARPS * KP * 8 + kStageBytes + (kSurvivorCap + 2) * 8;
@@ -106,6 +109,10 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.kth_out = a.kth_out;
   p.stride = a.stride > 0 ? a.stride : list_width(a.k);
   p.lens = a.lens;
+  // Short lists (a prefix of K valid keys, or fewer): stage 32 keys of each
+  // (the rest is read from L2 if it survives), so that the CTA's shared
+  // memory stays small and all queries run in one wave.
+  p.stage_keys = a.short_lists ? std::min(kStageKeys, std::max(2 * a.k, a.lists * 32)) : kStageKeys;
   // One query: a wide CTA to shorten the single merge. Many queries: 8-warp
   // CTAs, so that several fit on each SM and all queries run in one wave.
   if (a.queries >= kManyQueries) {

@@ -56,6 +56,7 @@ struct MergeLaunch {
   uint64_t* kth_out = nullptr;  // optional: each query's K-th key
   int stride = 0;               // keys from one list to the next (0: list_width(k))
   const int* lens = nullptr;    // optional [queries x lists] valid keys per list (else all stride)
+  int short_lists = 0;          // 1: lists hold few valid keys (K > 32): stage a 32-key prefix of each
 };
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
 
@@ -122,10 +123,12 @@ struct GemmSelectLaunch {
   int grid;                  // even: 2 x min(ceil(n / 256), SMs / 2); also the lists per query
   uint64_t timeout_ns;
   const uint64_t* theta0;    // optional per-query lower bound on the K-th key (keys >= it are kept)
-  int bound_mode = 0;        // 1: no selection; each CTA writes, per query, the best key of each of 4
-                             // chunks of its rows (chunk c: rows 32c..32c+31 of each of its tiles),
-                             // best first, then zeros
+  int bound_mode = 0;        // 1: no selection; each list (query, CTA, column half) holds the best key
+                             // of each of 4 chunks of its rows (chunk c: columns 32c..32c+31 of its
+                             // half of each tile), best first, then zeros
   int* lens = nullptr;       // K > 32: [queries][grid] valid keys of each list (required)
+  int wait_inputs = 1;       // 1: the kernel launched just before wrote the queries (the producer waits
+                             // for it); 0: the corpus stream may start while that kernel finishes
 };
 int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.

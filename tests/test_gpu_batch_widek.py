@@ -202,3 +202,24 @@ def test_full_size_planted_k100(rbf):
             q16 = oracle.round_bf16(qs[j])
             check_float_topk(idx[j], sc[j], oracle.scores(c16, q16), k, tol_abs=BF16_ACC_ABS)
             check_float_topk(idx[j], sc[j], oracle.scores(c, qs[j]), k, tol_abs=BF16_ABS)
+
+
+@pytest.mark.parametrize("sample", [0, 256, 16_384, 49_152, 70_144])
+@pytest.mark.parametrize("k", [8, 32, 100])
+def test_sample_option_changes_nothing(rbf, sample, k):
+    """RBF_OPT_BATCH_SAMPLE picks the pre-pass rows (0: none; up to all of
+    N): the result is bit-identical to the automatic choice and exact."""
+    n, d, b = 70_144, 64, 12
+    c = workloads.dyadic_grid(n, d, seed=71)
+    qs = workloads.dyadic_grid(b, d, seed=72)
+    with engine(rbf, "bf16", n, d, b) as e:
+        e.upload_corpus_rowmajor(c)
+        ref_idx, ref_sc = e.search_resident_batch(qs, k)
+        e.set_option(rbf.RBF_OPT_BATCH_SAMPLE, sample)
+        idx, sc = e.search_resident_batch(qs, k)
+        assert np.array_equal(idx, ref_idx) and np.array_equal(sc, ref_sc)
+        for j in range(0, b, 5):
+            check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], k))
+        for bad in (-2, 100):
+            with pytest.raises(rbf.RbfError):
+                e.set_option(rbf.RBF_OPT_BATCH_SAMPLE, bad)
