@@ -236,6 +236,24 @@ __device__ __forceinline__ uint64_t list_get(const uint64_t (&L)[KP], int e) {
   return x;
 }
 
+// Write the warp's 32 lists of 32 keys (lane i's list is key_at(0..31) of
+// lane i, to dst of lane i; no write for a null dst) with one 256-byte store
+// of the warp per list instead of 32 scattered ones: the rows go through tr,
+// 32 x 33 keys of shared memory that nothing else uses now.
+template <typename KeyAt>
+__device__ __forceinline__ void store_lists32(uint64_t* tr, int lane, uint64_t* dst, KeyAt key_at) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) tr[lane * 33 + i] = key_at(i);
+  __syncwarp();
+#pragma unroll 4
+  for (int j = 0; j < 32; ++j) {
+    uint64_t* d = reinterpret_cast<uint64_t*>(
+        __shfl_sync(kFullMask, static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(dst)), j));
+    if (d) d[lane] = tr[j * 33 + lane];
+  }
+  __syncwarp();
+}
+
 // sc[j] for a warp-uniform j: a switch keeps the scores in registers (a
 // dynamically indexed register array would live in local memory).
 __device__ __forceinline__ float pick(const float (&sc)[32], int j) {
@@ -511,13 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
-      if (qlocal < p.q_count) {
-        uint64_t* dst = p.partials + (static_cast<size_t>(p.q_out0 + qlocal) * gridDim.x + blockIdx.x) * 32;
-#pragma unroll
-        for (int i = 0; i < KP; ++i) dst[i] = L[i];
-#pragma unroll
-        for (int i = KP; i < 32; ++i) dst[i] = 0ull;
-      }
+      // Every MMA has finished (the last accumulator was full), so the ring
+      // is free for the transposed list write.
+      uint64_t* dst = qlocal < p.q_count
+                          ? p.partials + (static_cast<size_t>(p.q_out0 + qlocal) * gridDim.x + blockIdx.x) * 32
+                          : nullptr;
+      store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane, dst,
+                    [&](int i) { return i < KP ? L[i] : 0ull; });
     }
   }
 
@@ -952,25 +970,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       cswap(best[0], best[2]);
       cswap(best[1], best[3]);
       cswap(best[1], best[2]);
-      if (live) {
-        uint64_t* dst = p.partials + list_id() * 32;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = best[i];
-#pragma unroll
-        for (int i = 4; i < 32; ++i) dst[i] = 0ull;
-      }
+      // Every MMA of the pair has finished (the last accumulator was full),
+      // so this CTA's ring is free for the transposed list write.
+      store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane,
+                    live ? p.partials + list_id() * 32 : nullptr, [&](int i) { return i < 4 ? best[i] : 0ull; });
     } else {
       if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
-      if (live) {
-        if constexpr (kWide) {
-          p.lens[list_id()] = len;
-        } else {
-          uint64_t* dst = p.partials + list_id() * 32;
-#pragma unroll
-          for (int i = 0; i < KP; ++i) dst[i] = L[i];
-#pragma unroll
-          for (int i = KP; i < 32; ++i) dst[i] = 0ull;
-        }
+      if constexpr (kWide) {
+        if (live) p.lens[list_id()] = len;
+      } else {
+        store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane,
+                      live ? p.partials + list_id() * 32 : nullptr, [&](int i) { return i < KP ? L[i] : 0ull; });
       }
     }
   }
