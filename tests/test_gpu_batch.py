@@ -131,8 +131,9 @@ def test_full_size_planted(rbf):
             check_float_topk(idx[j], sc[j], oracle.scores(c, qs[j]), k, tol_abs=BF16_ABS)
 
 
-# N >= 65,536 rows: the batched path first finds each query's K-th best key over
-# the first 16,384 rows and drops every key below it in the main pass.
+# N >= 65,536 rows: the batched path first takes, for each query, the K-th
+# largest of its 32-row chunk maxima over the first 16,384 rows (K <= 32) and
+# drops every key below it in the main pass.
 
 @pytest.mark.parametrize("k", [1, 8, 32])
 def test_sample_bound_dyadic_exact(rbf, k):
