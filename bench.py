@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-batched", action="store_true")
     ap.add_argument("--no-int32", action="store_true")
     ap.add_argument("--no-cosine", action="store_true")
+    ap.add_argument("--no-views", action="store_true")
     ap.add_argument("--schedule", type=int, default=None)
     ap.add_argument("--ctas-per-sm", type=int, default=None)
     ap.add_argument("--stage-bytes", type=int, default=None)
@@ -341,6 +342,48 @@ def run_cosine(rbf, c, qs, planted, steps, warmup):
             "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "launches_per_step": 2, "steps": len(ms)}
 
 
+def run_views(rbf, reps=6):
+    """Concurrent single-query searches through views (rbf_create_view):
+    N=100,000 x D=768 fp32 (307 MB, larger than L2), K=8, 256 device-resident
+    queries per round issued round-robin over 1 or 4 handles, each on its own
+    stream; throughput = queries / host wall time of whole rounds (the calls
+    are asynchronous; one synchronisation per round)."""
+    import torch
+    import workloads
+    n, d, k, nq = 100_000, 768, 8, 256
+    c = workloads.unit_corpus(n, d, seed=1)
+    dq = torch.from_numpy(workloads.unit_queries(nq, d, seed=2)).cuda()
+    oi = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    osc = torch.empty((nq, k), dtype=torch.float32, device="cuda")
+    hbm, _ = hbm_peak()
+    out = {"workload": "N=100,000 x D=768 fp32, K=8, 256 queries per round, round-robin over handles"}
+    for nh in (1, 4):
+        streams = [torch.cuda.Stream() for _ in range(nh)]
+        base = rbf.Engine(n, d, k, stream=streams[0])
+        base.upload_corpus_rowmajor(c)
+        hs = [base] + [base.view(stream=st) for st in streams[1:]]
+
+        def round_():
+            for j in range(nq):
+                hs[j % nh].search_resident_dev(dq[j], k, oi[j], osc[j])
+
+        for _ in range(3):
+            round_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            round_()
+        torch.cuda.synchronize()
+        qps = reps * nq / (time.perf_counter() - t0)
+        for h in hs[1:]:
+            h.close()
+        base.close()
+        out[f"handles_{nh}"] = {"qps": round(qps, 1), "gbs": round(qps * n * d * 4 / 1e9, 1),
+                                "hbm_frac": round(qps * n * d * 4 / 1e9 / hbm, 4)}
+    out["speedup_4_over_1"] = round(out["handles_4"]["qps"] / out["handles_1"]["qps"], 3)
+    return out
+
+
 def run_int32(rbf, steps, warmup):
     """Flat int32 two-stage top-K: 100,000,000 values, K=20 and K=50."""
     import torch
@@ -501,6 +544,7 @@ def main():
     batched = run_batched(rbf, 30, 3) if (rank == 0 and not args.no_batched) else None
     batched_tf32 = run_batched(rbf, 20, 3, tf32=True) if (rank == 0 and not args.no_batched) else None
     int32 = run_int32(rbf, 50, 5) if (rank == 0 and not args.no_int32) else None
+    views = run_views(rbf) if (rank == 0 and not args.no_views) else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -529,6 +573,8 @@ def main():
             line["batched_tf32"] = batched_tf32
         if int32 is not None:
             line["int32"] = int32
+        if views is not None:
+            line["views"] = views
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

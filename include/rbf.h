@@ -102,7 +102,26 @@ typedef enum rbf_option {
 rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_batch,
                       uint32_t flags, void* cuda_stream, rbf_engine** out);
 
-/* Synchronise the engine's stream and free everything it owns. NULL is a no-op. */
+/* A second handle on `base`'s resident corpus, with its own stream and its
+ * own per-call buffers (partial lists, counters, error words, query staging,
+ * pinned result block, captured graphs) but no copy of the corpus: calls on
+ * different handles of one corpus may run at the same time, from different
+ * host threads and on different streams. One engine alone is not safe for
+ * concurrent calls (GPU-Resident Top-K for Agentic RAG, section 9, names
+ * that as a limitation; CUDA programming model series 9, section 4.2, runs
+ * independent top-K work on separate streams). The view takes the base's
+ * sizes, flags and options; set_option on a view changes only the view.
+ * An upload on the base is seen by its views at their next call; it must not
+ * overlap a call on any view. Views cannot upload.
+ *   base         an engine made by rbf_create (not a view)
+ *   cuda_stream  a cudaStream_t, or NULL for a view-owned non-blocking stream
+ *   out          receives the view handle (destroy it with rbf_destroy,
+ *                before the base)
+ * Errors: INVALID_VALUE (base NULL or a view, out NULL), OUT_OF_MEMORY, CUDA. */
+rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out);
+
+/* Synchronise the engine's stream and free everything it owns. NULL is a no-op.
+ * Errors: INVALID_VALUE (an engine that still has views). */
 rbf_status rbf_destroy(rbf_engine* engine);
 
 /* The cudaStream_t the engine runs on. */
@@ -136,7 +155,8 @@ rbf_status rbf_check_device_error(rbf_engine* engine);
  * multiple of 4 floats and zero-padded; with RBF_FLAG_BF16_CORPUS a bf16 copy
  * (round-to-nearest-even) is made too. A new upload replaces the old corpus.
  * Blocks until the copy is complete.
- * Errors: INVALID_VALUE (N < 1, N > max_n, D < 1, D > max_d, corpus NULL). */
+ * Errors: INVALID_VALUE (N < 1, N > max_n, D < 1, D > max_d, corpus NULL, a
+ * view). */
 rbf_status upload_corpus_rowmajor(rbf_engine* engine, const float* corpus, int64_t n, int32_t d);
 
 /* ---------------------------------------------------------- single query */

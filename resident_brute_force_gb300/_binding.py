@@ -47,6 +47,7 @@ _U64 = ctypes.c_uint64
 _S = ctypes.c_int
 SIGNATURES = {
     "rbf_create": (_S, [_I64, _I32, _I32, _I32, _U32, _P, ctypes.POINTER(_P)]),
+    "rbf_create_view": (_S, [_P, _P, ctypes.POINTER(_P)]),
     "rbf_destroy": (_S, [_P]),
     "rbf_stream": (_P, [_P]),
     "rbf_num_sms": (_I32, [_P]),
@@ -150,26 +151,41 @@ class Engine:
     """An engine with every buffer preallocated (see ``rbf_create``)."""
 
     def __init__(self, max_n: int, max_d: int, max_k: int = RBF_MAX_K, max_batch: int = 1,
-                 flags: int = 0, stream=None):
+                 flags: int = 0, stream=None, _view_of=None):
         self.lib = load_library()
         handle = ctypes.c_void_p()
         s = None
         if stream is not None:
             s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-        st = self.lib.rbf_create(int(max_n), int(max_d), int(max_k), int(max_batch), int(flags),
-                                 ctypes.c_void_p(s) if s else None, ctypes.byref(handle))
+        if _view_of is not None:
+            st = self.lib.rbf_create_view(_view_of._h, ctypes.c_void_p(s) if s else None, ctypes.byref(handle))
+            where = "rbf_create_view"
+        else:
+            st = self.lib.rbf_create(int(max_n), int(max_d), int(max_k), int(max_batch), int(flags),
+                                     ctypes.c_void_p(s) if s else None, ctypes.byref(handle))
+            where = "rbf_create"
         if st != RBF_OK:
-            raise RbfError(st, "rbf_create")
+            raise RbfError(st, where)
         self._h = handle
         self._stream_ref = stream
-        self.d = None
-        self.n = None
+        self._base = _view_of  # a view keeps its base alive
+        self.d = _view_of.d if _view_of is not None else None
+        self.n = _view_of.n if _view_of is not None else None
+
+    def view(self, stream=None) -> "Engine":
+        """A second handle on this engine's resident corpus with its own stream
+        and per-call buffers (rbf_create_view): calls on different handles may
+        run concurrently. Close views before their base."""
+        return Engine(0, 0, _view_of=self, stream=stream)
 
     # -- lifetime
     def close(self) -> None:
         if getattr(self, "_h", None):
-            self.lib.rbf_destroy(self._h)
+            st = self.lib.rbf_destroy(self._h)
+            if st != RBF_OK:
+                raise RbfError(st, "rbf_destroy (close the views first)")
             self._h = None
+            self._base = None
 
     def __del__(self):
         try:

@@ -102,6 +102,15 @@ struct rbf_engine {
   int last_cuda_error = 0;
   int fault_kind = 0;
   int fault_count = 0;
+
+  // Views (rbf_create_view): a view searches its owner's corpus with its own
+  // stream and per-call buffers. The owner counts its views and bumps
+  // corpus_version around every upload; a view re-reads the corpus state
+  // when the version it saw is stale.
+  rbf_engine* owner = nullptr;
+  int views = 0;
+  unsigned corpus_version = 0;
+  unsigned seen_version = 0;
 };
 
 namespace {
@@ -256,8 +265,12 @@ void release(rbf_engine* e) {
   if (!e) return;
   if (e->stream) cudaStreamSynchronize(e->stream);
   drop_graphs(e);
-  cudaFree(e->corpus);
-  cudaFree(e->corpus_bf16);
+  if (e->owner) {
+    --e->owner->views;  // the corpus belongs to the owner
+  } else {
+    cudaFree(e->corpus);
+    cudaFree(e->corpus_bf16);
+  }
   cudaFree(e->query_bf16);
   cudaFree(e->query_f32);
   cudaFree(e->theta0);
@@ -272,6 +285,74 @@ void release(rbf_engine* e) {
   cudaFreeHost(e->h_result);
   if (e->own_stream && e->stream) cudaStreamDestroy(e->stream);
   delete e;
+}
+
+// Every per-call buffer of an engine or a view (not the corpus). On failure
+// the engine is released.
+rbf_status alloc_call_buffers(rbf_engine* e) {
+  bool ok = true;
+  if (e->flags & RBF_FLAG_BF16_CORPUS)
+    ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
+  else
+    ok = ok && cudaMalloc(&e->query_f32, static_cast<size_t>(e->query_rows) * e->max_pitch * 4) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(e->max_batch) * sizeof(uint64_t)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->lens, static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms * sizeof(int)) ==
+                 cudaSuccess;
+  ok = ok && cudaMalloc(&e->query, static_cast<size_t>(e->max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->counters, 8 * sizeof(unsigned)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->i32_theta0, sizeof(uint64_t)) == cudaSuccess;
+  ok = ok && cudaMalloc(&e->result, e->result_bytes) == cudaSuccess;
+  ok = ok &&
+       cudaMallocHost(&e->h_query, static_cast<size_t>(e->max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMallocHost(&e->h_result, e->result_bytes) == cudaSuccess;
+  ok = ok && cudaHostGetDevicePointer(reinterpret_cast<void**>(&e->d_hres), e->h_result, 0) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    release(e);
+    return RBF_ERR_OUT_OF_MEMORY;
+  }
+  ok = cudaMemsetAsync(e->errw, 0, 4 * sizeof(int), e->stream) == cudaSuccess &&
+       cudaMemsetAsync(e->counters, 0, 8 * sizeof(unsigned), e->stream) == cudaSuccess &&
+       cudaMemsetAsync(e->query, 0, static_cast<size_t>(e->max_batch) * e->max_pitch * sizeof(float), e->stream) ==
+           cudaSuccess &&
+       cudaStreamSynchronize(e->stream) == cudaSuccess;
+  if (!ok) {
+    release(e);
+    return RBF_ERR_CUDA;
+  }
+  return RBF_OK;
+}
+
+// A view takes its owner's corpus state (pointers, shape, readiness, corpus
+// tensor map) whenever the owner has uploaded since the view last looked, and
+// points its own query tensor map at its own query buffer. Its captured
+// graphs are dropped then (they carry the old shape).
+rbf_status sync_view(rbf_engine* e) {
+  const rbf_engine* o = e->owner;
+  if (!o || e->seen_version == o->corpus_version) return RBF_OK;
+  cudaStreamSynchronize(e->stream);
+  drop_graphs(e);
+  e->corpus = o->corpus;
+  e->corpus_bf16 = o->corpus_bf16;
+  e->n = o->n;
+  e->d = o->d;
+  e->pitch = o->pitch;
+  e->pitch_bf16 = o->pitch_bf16;
+  e->last_lists = 0;
+  e->last_k = 0;
+  e->tmaps_ready = false;
+  if (o->ready && o->tmaps_ready) {
+    e->tmap_corpus = o->tmap_corpus;
+    const bool ok = e->corpus_bf16 ? make_bf16_tensor_map(&e->tmap_query, e->query_bf16, e->query_rows, e->pitch_bf16)
+                                   : make_f32_tensor_map(&e->tmap_query, e->query_f32, e->query_rows, e->pitch);
+    if (!ok) return RBF_ERR_CUDA;
+    e->tmaps_ready = true;
+  }
+  e->ready = o->ready;
+  e->seen_version = o->corpus_version;
+  return RBF_OK;
 }
 
 }  // namespace
@@ -349,44 +430,61 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   bool ok = true;
   if (flags & RBF_FLAG_FP32_CORPUS)
     ok = ok && cudaMalloc(&e->corpus, static_cast<size_t>(max_n) * e->max_pitch * sizeof(float)) == cudaSuccess;
-  if (flags & RBF_FLAG_BF16_CORPUS) {
+  if (flags & RBF_FLAG_BF16_CORPUS)
     ok = ok && cudaMalloc(&e->corpus_bf16, align_up(static_cast<size_t>(max_n), 128) * e->max_pitch_bf16 * 2) ==
                    cudaSuccess;
-    ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
-  } else {
-    ok = ok && cudaMalloc(&e->query_f32, static_cast<size_t>(e->query_rows) * e->max_pitch * 4) == cudaSuccess;
-  }
-  ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(max_batch) * sizeof(uint64_t)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->lens, static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms * sizeof(int)) ==
-                 cudaSuccess;
-  ok = ok && cudaMalloc(&e->query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->counters, 8 * sizeof(unsigned)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->i32_theta0, sizeof(uint64_t)) == cudaSuccess;
-  ok = ok && cudaMalloc(&e->result, e->result_bytes) == cudaSuccess;
-  ok = ok && cudaMallocHost(&e->h_query, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
-  ok = ok && cudaMallocHost(&e->h_result, e->result_bytes) == cudaSuccess;
-  ok = ok && cudaHostGetDevicePointer(reinterpret_cast<void**>(&e->d_hres), e->h_result, 0) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     release(e);
     return RBF_ERR_OUT_OF_MEMORY;
   }
-  ok = cudaMemsetAsync(e->errw, 0, 4 * sizeof(int), e->stream) == cudaSuccess &&
-       cudaMemsetAsync(e->counters, 0, 8 * sizeof(unsigned), e->stream) == cudaSuccess &&
-       cudaMemsetAsync(e->query, 0, static_cast<size_t>(max_batch) * e->max_pitch * sizeof(float), e->stream) ==
-           cudaSuccess &&
-       cudaStreamSynchronize(e->stream) == cudaSuccess;
-  if (!ok) {
+  if (rbf_status st2 = alloc_call_buffers(e)) return st2;  // releases e on failure
+  *out = e;
+  return RBF_OK;
+}
+
+rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out) {
+  if (!base || base->owner || !out) return RBF_ERR_INVALID_VALUE;
+  rbf_engine* e = new (std::nothrow) rbf_engine();
+  if (!e) return RBF_ERR_OUT_OF_MEMORY;
+  e->device = base->device;
+  e->num_sms = base->num_sms;
+  e->smem_optin = base->smem_optin;
+  e->max_n = base->max_n;
+  e->max_d = base->max_d;
+  e->max_k = base->max_k;
+  e->max_batch = base->max_batch;
+  e->flags = base->flags;
+  e->max_pitch = base->max_pitch;
+  e->max_pitch_bf16 = base->max_pitch_bf16;
+  e->query_rows = base->query_rows;
+  e->partials_cap = base->partials_cap;
+  e->result_bytes = base->result_bytes;
+  e->ctas_per_sm = base->ctas_per_sm;
+  e->stage_bytes = base->stage_bytes;
+  e->smem_budget = base->smem_budget;
+  e->timeout_ns = base->timeout_ns;
+  e->dynamic = base->dynamic;
+  e->batch_sample = base->batch_sample;
+  e->owner = base;
+  e->seen_version = base->corpus_version - 1;  // read the corpus state at the first call
+  ++base->views;
+  if (cuda_stream) {
+    e->stream = static_cast<cudaStream_t>(cuda_stream);
+  } else if (cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking) != cudaSuccess) {
+    e->stream = nullptr;
     release(e);
     return RBF_ERR_CUDA;
+  } else {
+    e->own_stream = true;
   }
+  if (rbf_status st = alloc_call_buffers(e)) return st;
   *out = e;
   return RBF_OK;
 }
 
 rbf_status rbf_destroy(rbf_engine* e) {
+  if (e && e->views > 0) return RBF_ERR_INVALID_VALUE;
   release(e);
   return RBF_OK;
 }
@@ -396,7 +494,7 @@ void* rbf_stream(const rbf_engine* e) { return e ? static_cast<void*>(e->stream)
 int32_t rbf_num_sms(const rbf_engine* e) { return e ? e->num_sms : 0; }
 
 int32_t rbf_num_partials(const rbf_engine* e) {
-  if (!e || !e->ready) return 0;
+  if (!e || sync_view(const_cast<rbf_engine*>(e)) != RBF_OK || !e->ready) return 0;
   ScoreShape sh;
   return score_shape(e, 1, &sh) ? sh.grid : 0;
 }
@@ -448,9 +546,10 @@ rbf_status rbf_check_device_error(rbf_engine* e) {
 }
 
 rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n, int32_t d) {
-  if (!e || !corpus || n < 1 || n > e->max_n || d < 1 || d > e->max_d) return RBF_ERR_INVALID_VALUE;
+  if (!e || !corpus || n < 1 || n > e->max_n || d < 1 || d > e->max_d || e->owner) return RBF_ERR_INVALID_VALUE;
   if (!e->corpus) return RBF_ERR_UNSUPPORTED;
   e->ready = false;
+  ++e->corpus_version;  // views re-read the corpus state at their next call
   cudaStreamSynchronize(e->stream);
   drop_graphs(e);  // captured launches carry the old corpus shape
   const int pitch = static_cast<int>(align_up(static_cast<size_t>(d), 4));
@@ -490,11 +589,13 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
   e->ready = true;
   e->last_lists = 0;
   e->last_k = 0;
+  ++e->corpus_version;
   return RBF_OK;
 }
 
 rbf_status score_select_partials_dev(rbf_engine* e, const float* d_query, int32_t k) {
   if (!e || !d_query) return RBF_ERR_INVALID_VALUE;
+  if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
   return enqueue_score(e, d_query, k);
@@ -502,6 +603,7 @@ rbf_status score_select_partials_dev(rbf_engine* e, const float* d_query, int32_
 
 rbf_status merge_partial_topk_dev(rbf_engine* e, int32_t k, int32_t* d_idx, float* d_score) {
   if (!e || !d_idx || !d_score) return RBF_ERR_INVALID_VALUE;
+  if (rbf_status s = sync_view(e)) return s;
   if (!e->ready || e->last_lists == 0) return RBF_ERR_NOT_READY;
   if (k != e->last_k) return RBF_ERR_INVALID_VALUE;
   return enqueue_merge(e, k, e->last_lists, 1, 0, d_idx, d_score, reinterpret_cast<int*>(e->result));
@@ -509,6 +611,7 @@ rbf_status merge_partial_topk_dev(rbf_engine* e, int32_t k, int32_t* d_idx, floa
 
 rbf_status search_resident_dev(rbf_engine* e, const float* d_query, int32_t k, int32_t* d_idx, float* d_score) {
   if (!e || !d_query || !d_idx || !d_score) return RBF_ERR_INVALID_VALUE;
+  if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
   if (rbf_status s = enqueue_score(e, d_query, k)) return s;
@@ -549,6 +652,7 @@ static rbf_status capture_host_search(rbf_engine* e, int k, const ResultLayout& 
 
 rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t* out_idx, float* out_score) {
   if (!e || !query || !out_idx || !out_score) return RBF_ERR_INVALID_VALUE;
+  if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
   std::memcpy(e->h_query, query, static_cast<size_t>(e->d) * 4);
@@ -709,6 +813,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
 rbf_status search_resident_batch_dev(rbf_engine* e, const float* d_queries, int32_t b, int32_t k, int32_t* d_idx,
                                      float* d_score) {
   if (!e || !d_queries || !d_idx || !d_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
+  if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
   return enqueue_batch(e, d_queries, b, k, d_idx, d_score, reinterpret_cast<int*>(e->result));
@@ -717,6 +822,7 @@ rbf_status search_resident_batch_dev(rbf_engine* e, const float* d_queries, int3
 rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b, int32_t k, int32_t* out_idx,
                                  float* out_score) {
   if (!e || !queries || !out_idx || !out_score || b < 1 || b > e->max_batch) return RBF_ERR_INVALID_VALUE;
+  if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
   const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
