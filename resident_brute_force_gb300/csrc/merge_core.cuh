@@ -16,10 +16,11 @@
 // the number of lists, the m-th largest t-th key X has m lists each holding t
 // keys >= X, so at least K keys are >= X; and each list's K-th key is itself
 // such a bound. Only the keys >= B can be in the answer (in each best-first
-// list they form a prefix); they are gathered, and each one's place is the
-// number of gathered keys greater than it (keys are distinct). On random data
-// a few more than K keys survive. If more than kSurvivorCap survive, or there
-// are too many lists, the general merge runs instead: the lists are staged
+// list they form a prefix); they are gathered (one list per thread), and each
+// one's place is the number of gathered keys greater than it (keys are
+// distinct). On random data a few more than K keys survive. If more than
+// kSurvivorCap survive, or there are too many lists, the general merge runs
+// instead: the lists are staged
 // in groups, each warp folds a strided subset of them into a register bitonic
 // list (reversed max + bitonic merge per list), the warp lists are merged
 // pairwise in shared memory and warp 0 writes the best K decoded.
@@ -155,6 +156,7 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
     int greater = 0;
     if (l < L) {
       x = row[l];
+#pragma unroll 4
       for (int j = part; j < L; j += 8) greater += row[j] > x ? 1 : 0;
     }
     greater += __shfl_xor_sync(kFullMask, greater, 1);
@@ -170,22 +172,31 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
   const uint64_t bound = s_bound;
 
   // Gather each list's prefix of keys >= bound (lists are best first, so
-  // the prefix ends at the first key below it); keys past the staged ones
-  // are read from L2.
-  for (int l = warp; l < L; l += WARPS) {
-    for (int e0 = 0; e0 < k; e0 += 32) {
-      const int e = e0 + lane;
-      uint64_t key = 0;
-      if (e < k) key = e < P ? stage[l * P + e] : list_key(p, base, l, e);
-      const bool pass = key >= bound;
-      const unsigned msk = __ballot_sync(kFullMask, pass);
-      if (msk == 0) break;
-      int at = 0;
-      if (lane == 0) at = atomicAdd(&s_count, __popc(msk));
-      at = __shfl_sync(kFullMask, at, 0) + __popc(msk & ((1u << lane) - 1u));
-      if (pass && at < kSurvivorCap) surv[at] = key;
-      if (msk != kFullMask) break;
+  // the prefix ends at the first key below it), one list per thread: the
+  // thread counts its prefix, a warp scan turns the counts into offsets
+  // behind one shared atomic per warp, and the thread copies its keys. Keys
+  // past the staged ones are read from L2.
+  for (int l0 = 0; l0 < L; l0 += NT) {
+    const int l = l0 + tid;
+    int c = 0;
+    if (l < L) {
+      while (c < k) {
+        const uint64_t key = c < P ? stage[l * P + c] : list_key(p, base, l, c);
+        if (key < bound) break;
+        ++c;
+      }
     }
+    int incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFullMask, incl, d);
+      if (lane >= d) incl += y;
+    }
+    int at = 0;
+    if (lane == 31 && incl > 0) at = atomicAdd(&s_count, incl);
+    at = __shfl_sync(kFullMask, at, 31) + incl - c;
+    for (int i = 0; i < c; ++i, ++at)
+      if (at < kSurvivorCap) surv[at] = i < P ? stage[l * P + i] : list_key(p, base, l, i);
   }
   __syncthreads();
   const int S = s_count;
