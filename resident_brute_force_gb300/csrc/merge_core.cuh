@@ -13,7 +13,8 @@
 // are staged in shared memory by all threads at once, one round trip to L2. A
 // lower bound B on the global K-th key then comes from two rows of the staged
 // lists: with t the smallest power of two for which m = ceil(K/t) is at most
-// the number of lists, the m-th largest t-th key X has m lists each holding t
+// the number of lists, the m-th largest t-th key X (found by ranking each
+// t-th key against warp-sorted runs of them) has m lists each holding t
 // keys >= X, so at least K keys are >= X; and each list's K-th key is itself
 // such a bound. Only the keys >= B can be in the answer (in each best-first
 // list they form a prefix); they are gathered (one list per thread), and each
@@ -59,7 +60,7 @@ __device__ __forceinline__ uint64_t list_key(const MergeOut& p, const uint64_t* 
 }
 
 constexpr int kSurvivorCap = 2048;  // keys gathered by the fast path
-constexpr int kFastMaxLists = 512;  // lists the bound selection handles (its work grows as lists^2)
+constexpr int kFastMaxLists = 512;  // lists the bound selection handles (its work grows as lists^2 / 32)
 
 __device__ __forceinline__ void emit(const MergeOut& p, int e, uint64_t key) {
   const size_t o = p.q * static_cast<size_t>(p.k) + e;
@@ -144,29 +145,33 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
   }
   stage_heads<NT>(p, stage, base, 0, L, P);
   __syncthreads();
-  uint64_t* row = surv;  // the lists' t-th keys, contiguous (the survivors come later)
-  for (int l = tid; l < L; l += NT) row[l] = stage[l * P + t - 1];
+  // The lists' t-th keys in runs of 32, each sorted best first by one warp
+  // (they sit where the survivors go later; the last run is padded with the
+  // empty key).
+  uint64_t* row = surv;
+  const int runs = (L + 31) >> 5;
+  for (int r = warp; r < runs; r += WARPS) {
+    const int l = r * 32 + lane;
+    row[l] = warp_sort32_desc(l < L ? stage[l * P + t - 1] : 0ull, lane);
+  }
   __syncthreads();
 
-  // Eight lanes per list: the count of lists whose t-th key beats this one's.
-  for (int i0 = 0; i0 < L * 8; i0 += NT) {
-    const int l = (i0 + tid) >> 3;
-    const int part = tid & 7;
-    uint64_t x = 0;
+  // One list per thread: the number of lists whose t-th key beats this one's
+  // is the sum over the runs of a 5-step binary search (keys are distinct,
+  // except empty ones, which beat nothing).
+  for (int l = tid; l < L; l += NT) {
+    const uint64_t x = stage[l * P + t - 1];
     int greater = 0;
-    if (l < L) {
-      x = row[l];
-#pragma unroll 4
-      for (int j = part; j < L; j += 8) greater += row[j] > x ? 1 : 0;
+    for (int r = 0; r < runs; ++r) {
+      const uint64_t* run = row + r * 32;
+      int lo = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) lo += run[lo + step - 1] > x ? step : 0;
+      greater += lo + (run[lo] > x ? 1 : 0);
     }
-    greater += __shfl_xor_sync(kFullMask, greater, 1);
-    greater += __shfl_xor_sync(kFullMask, greater, 2);
-    greater += __shfl_xor_sync(kFullMask, greater, 4);
-    if (l < L && part == 0) {
-      uint64_t b = k <= P ? stage[l * P + k - 1] : list_key(p, base, l, k - 1);
-      if (greater == m - 1) b = umax64(b, x);
-      atomicMax(&s_bound, static_cast<unsigned long long>(b));
-    }
+    uint64_t b = k <= P ? stage[l * P + k - 1] : list_key(p, base, l, k - 1);
+    if (greater == m - 1) b = umax64(b, x);
+    atomicMax(&s_bound, static_cast<unsigned long long>(b));
   }
   __syncthreads();
   const uint64_t bound = s_bound;
