@@ -102,13 +102,23 @@ __device__ __forceinline__ void stage_heads(const MergeOut& p, uint64_t* dst, co
   }
 }
 
+// The row t of the bound: the smallest power of two with ceil(K/t) <= lists,
+// at most K.
+__host__ __device__ constexpr int fast_row(int lists, int k) {
+  int t = 1;
+  while ((k + t - 1) / t > lists) t <<= 1;
+  return t < k ? t : k;
+}
+
 // Keys of each list the fast path stages, given room for stage_keys keys:
-// all K if they fit, else the largest multiple of 32 that does (at least 32);
-// 0 if the fast path does not apply.
+// min(K, max(32, t)) if they fit (survivors rarely reach further into a
+// list; those that do are read from L2), else the largest multiple of 32
+// that does (at least 32); 0 if the fast path does not apply.
 __host__ __device__ constexpr int fast_prefix(int lists, int k, int stage_keys) {
-  return lists > kFastMaxLists ? 0
-         : lists * k <= stage_keys ? k
-         : (stage_keys / lists) & ~31;
+  if (lists > kFastMaxLists) return 0;
+  const int t = fast_row(lists, k);
+  const int want = k < (t > 32 ? t : 32) ? k : (t > 32 ? t : 32);
+  return lists * want <= stage_keys ? want : (stage_keys / lists) & ~31;
 }
 
 // Shared memory (bytes) the fast path needs: the staged prefixes and the
@@ -129,9 +139,7 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
   const int k = p.k;
   const int P = fast_prefix(L, k, stage_keys);  // staged keys per list
   if (P < 1 || (P < k && P < 32)) return false;
-  int t = 1;
-  while ((k + t - 1) / t > L) t <<= 1;
-  t = min(t, k);  // t = K gives m = 1, which every list count satisfies
+  const int t = fast_row(L, k);  // t = K gives m = 1, which every list count satisfies
   if (t > P) return false;
   const int m = (k + t - 1) / t;
   const int tid = threadIdx.x;
@@ -177,20 +185,17 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
   const uint64_t bound = s_bound;
 
   // Gather each list's prefix of keys >= bound (lists are best first, so
-  // the prefix ends at the first key below it), one list per thread: the
-  // thread counts its prefix, a warp scan turns the counts into offsets
-  // behind one shared atomic per warp, and the thread copies its keys. Keys
-  // past the staged ones are read from L2.
+  // the prefix ends at the first key below it), one list per thread within
+  // the staged keys: the thread counts its prefix, a warp scan turns the
+  // counts into offsets behind one shared atomic per warp, and the thread
+  // copies its keys. A prefix that runs past the staged keys (rare) is
+  // continued from L2 by the whole warp, 32 keys per round trip.
   for (int l0 = 0; l0 < L; l0 += NT) {
     const int l = l0 + tid;
+    const int lim = min(P, k);
     int c = 0;
-    if (l < L) {
-      while (c < k) {
-        const uint64_t key = c < P ? stage[l * P + c] : list_key(p, base, l, c);
-        if (key < bound) break;
-        ++c;
-      }
-    }
+    if (l < L)
+      while (c < lim && stage[l * P + c] >= bound) ++c;
     int incl = c;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -201,7 +206,25 @@ __device__ bool merge_fast(const MergeOut& p, const uint64_t* base, int L, uint6
     if (lane == 31 && incl > 0) at = atomicAdd(&s_count, incl);
     at = __shfl_sync(kFullMask, at, 31) + incl - c;
     for (int i = 0; i < c; ++i, ++at)
-      if (at < kSurvivorCap) surv[at] = i < P ? stage[l * P + i] : list_key(p, base, l, i);
+      if (at < kSurvivorCap) surv[at] = stage[l * P + i];
+    unsigned more = __ballot_sync(kFullMask, l < L && c == lim && lim < k);
+    while (more) {
+      const int src = __ffs(more) - 1;
+      more &= more - 1;
+      const int lm = l0 + warp * 32 + src;
+      for (int e0 = lim; e0 < k; e0 += 32) {
+        const int e = e0 + lane;
+        const uint64_t key = e < k ? list_key(p, base, lm, e) : 0ull;
+        const bool pass = key >= bound;
+        const unsigned msk = __ballot_sync(kFullMask, pass);
+        if (msk == 0) break;
+        int a = 0;
+        if (lane == 0) a = atomicAdd(&s_count, __popc(msk));
+        a = __shfl_sync(kFullMask, a, 0) + __popc(msk & ((1u << lane) - 1u));
+        if (pass && a < kSurvivorCap) surv[a] = key;
+        if (msk != kFullMask) break;
+      }
+    }
   }
   __syncthreads();
   const int S = s_count;
