@@ -996,15 +996,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // --------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -1012,12 +1012,10 @@ template <int KP, bool TF32>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
   auto fn = gemm_select_kernel<KP, TF32>;
   const int smem = gemm_select_smem_bytes();
-  static int configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  // Set once per instance (a function-local static is initialised once, even
+  // with callers on several host threads).
+  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (limit != cudaSuccess) return limit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -1039,12 +1037,8 @@ template <int KP, bool TF32>
 cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
   auto fn = gemm_select_pair_kernel<KP, TF32>;
   const int smem = pair_smem_bytes();
-  static int configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (limit != cudaSuccess) return limit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);

@@ -12,6 +12,18 @@ constexpr int kScoreConsumerWarps = 8;
 // Warps of the int32 stage-1 kernel.
 constexpr int kI32Warps = 16;
 
+// The current device's opt-in dynamic shared-memory limit per block (read
+// once).
+inline int max_dynamic_smem() {
+  static const int v = [] {
+    int dev = 0, bytes = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&bytes, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return bytes;
+  }();
+  return v;
+}
+
 // Candidate-list width for a K: the smallest power of two >= max(K, 32).
 inline int list_width(int k) {
   int kp = 32;

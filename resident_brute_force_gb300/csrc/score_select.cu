@@ -299,12 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
 template <int KP, int NCH, bool NORM>
 cudaError_t launch_t(const Params& p, int grid, int smem, cudaStream_t stream) {
   auto fn = score_select_f32_kernel<KP, NCH, NORM>;
-  static int configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  // The launch size depends on the engine's options (at most the device's
+  // opt-in limit), so the limit is raised once to that maximum
+  // (thread-safe static).
+  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        max_dynamic_smem());
+  if (limit != cudaSuccess) return limit;
   fn<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -475,12 +475,8 @@ constexpr int kStreamSmem = kSStages * kSTileBytes + kSStages * 32 + kSW * stati
 template <int KP>
 cudaError_t launch_stream_t(const StreamParams& p, int grid, cudaStream_t stream) {
   auto fn = topk_i32_stream_kernel<KP>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem);
+  if (limit != cudaSuccess) return limit;
   fn<<<grid, kSThreads, kStreamSmem, stream>>>(p);
   return cudaGetLastError();
 }
