@@ -4,8 +4,9 @@
 Workload: N = 1,000,000 corpus rows, D = 1024, fp32, unit-norm Gaussian rows
 (seed 1), 1,000 unit-norm queries (seed 2), 10 planted near-duplicates per
 query (seed 3), inner product, K = 8 (headline) with K = 32 and K = 100 timed
-in their own regions. One step = one query: the fused scoring kernel and the
-merge kernel. The corpus (4.1 GB) is larger than L2, so no flush is needed.
+in their own regions. One step = one query = one launch of the fused scoring
+kernel (scores, per-CTA selection, and the merge in its last CTA). The corpus
+(4.1 GB) is larger than L2, so no flush is needed.
 
 Prints one JSON line. ``value`` is the achieved corpus-read rate in GB/s over
 the K = 8 timed steps (algorithmic bytes N*D*4 per step / device time).
@@ -30,7 +31,6 @@ sys.path.insert(0, ROOT)
 
 METRIC = "search p50 µs & achieved HBM GB/s (vs 8 TB/s) at N=1M D=1024 K=8/32/100"
 FALLBACK_HBM_GBS = 6800.0
-K1_SAMPLE = 8  # time the scoring kernel alone on every 8th step
 WORKLOAD = ("single-query resident search: N=1,000,000 x D=1024 fp32 unit-norm Gaussian corpus "
             "(4.1 GB resident), 1,000 queries with 10 planted near-duplicates each, inner product, K=8")
 
@@ -90,7 +90,7 @@ def hbm_peak():
 def kernel_source_hash() -> str:
     """Hash of the files that define the scoring kernel's code."""
     h = hashlib.sha256()
-    for f in ("score_select.cu", "rbf_device.cuh"):
+    for f in ("score_select.cu", "rbf_device.cuh", "merge_core.cuh"):
         with open(os.path.join(ROOT, "resident_brute_force_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -339,7 +339,7 @@ def run_cosine(rbf, c, qs, planted, steps, warmup):
     gbs = n * d * 4 / p50 / 1e9
     return {"workload": "cosine mode, N=1,000,000 x D=1024 fp32 (rows unit length at upload), K=8",
             "p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
-            "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "launches_per_step": 2, "steps": len(ms)}
+            "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "launches_per_step": 1, "steps": len(ms)}
 
 
 def run_views(rbf, reps=6):
@@ -476,38 +476,32 @@ def main():
         with torch.cuda.stream(stream):
             for j in range(args.warmup):
                 eng.search_resident_dev(dq[j % nq], k, d_idx, d_sc)
-        # Events at every step boundary; on every SAMPLE-th step one more
-        # event between the two kernels times the scoring kernel alone (an
-        # event there costs the merge its early launch, so only a sample).
+        # One step is one search_resident_dev call: a single launch of the
+        # scoring kernel, whose last CTA also merges the per-CTA lists. Events
+        # at every step boundary on the launching stream time each launch.
         bounds = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        mids = {j: torch.cuda.Event(enable_timing=True) for j in range(0, args.steps, K1_SAMPLE)}
         barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for j in range(args.steps):
                 bounds[j].record(stream)
-                eng.score_select_partials_dev(dq[j % nq], k)
-                if j in mids:
-                    mids[j].record(stream)
-                eng.merge_partial_topk_dev(k, d_idx, d_sc)
+                eng.search_resident_dev(dq[j % nq], k, d_idx, d_sc)
             bounds[args.steps].record(stream)
         torch.cuda.synchronize()
         barrier()
         step_ms = [bounds[j].elapsed_time(bounds[j + 1]) for j in range(args.steps)]
-        k1_ms = [bounds[j].elapsed_time(mids[j]) for j in sorted(mids)]
         total_ms = max_over_ranks(bounds[0].elapsed_time(bounds[args.steps]), world)
         rec = {
             "p50_us": round(percentile(step_ms, 50) * 1e3, 2),
             "p99_us": round(percentile(step_ms, 99) * 1e3, 2),
             "gbs": round(world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9, 1),
             "qps": round(world * args.steps / (total_ms * 1e-3), 1),
-            "score_select_us_mean": round(statistics.mean(k1_ms) * 1e3, 2),
-            "score_select_launches_timed": len(k1_ms),
-            "merge_and_gap_us_mean": round((statistics.mean(step_ms) - statistics.mean(k1_ms)) * 1e3, 2),
+            "launch_us_mean": round(statistics.mean(step_ms) * 1e3, 2),
+            "launches_per_step": 1,
         }
         per_k[str(k)] = rec
         if k == 8:
-            headline = (total_ms, k1_ms, step_ms)
+            headline = (total_ms, step_ms)
     clocks = sampler.stop()
 
     # End to end through the public host-buffer call: pinned staging of the
@@ -529,10 +523,11 @@ def main():
                "p50_us": round(percentile(call_s, 50) * 1e6, 2), "p99_us": round(percentile(call_s, 99) * 1e6, 2),
                "ms_per_step": round(dt / args.steps * 1e3, 4)}
 
-    total_ms, k1_ms, step_ms = headline
+    total_ms, step_ms = headline
     value = world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
-    k1_mean_s = statistics.mean(k1_ms) * 1e-3
+    # The dominant (only) kernel's average launch duration: the mean step.
+    k1_mean_s = statistics.mean(step_ms) * 1e-3
     achieved = bytes_per_step / k1_mean_s / 1e9
     roofline = {"kernel": "score_select_f32", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -563,7 +558,7 @@ def main():
             "p50_us": per_k["8"]["p50_us"], "p99_us": per_k["8"]["p99_us"], "per_k": per_k,
             "k100_over_k8": round(per_k["100"]["p50_us"] / per_k["8"]["p50_us"], 3) if "100" in per_k else None,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 2 * args.steps, "clocks": clocks,
+            "gpu_launches": args.steps, "clocks": clocks,
         }
         if cosine is not None:
             line["cosine"] = cosine

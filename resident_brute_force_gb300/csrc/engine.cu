@@ -182,7 +182,11 @@ rbf_status check_k(const rbf_engine* e, int k) {
   return RBF_OK;
 }
 
-rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k) {
+// The scoring kernel over the resident corpus; with d_idx set its last CTA
+// also merges the lists into the outputs (one launch per search), else the
+// lists stay for enqueue_merge (last_lists). *merged tells which happened.
+rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_idx = nullptr,
+                         float* d_score = nullptr, int* result_err = nullptr, bool* merged = nullptr) {
   ScoreShape sh;
   if (!score_shape(e, k, &sh)) return RBF_ERR_UNSUPPORTED;
   if (static_cast<size_t>(sh.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
@@ -205,9 +209,17 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k) {
   // Cosine mode: rows are unit length already; the kernel scales its copy of
   // the query to unit length, so the inner product is the cosine.
   a.normalize_query = (e->flags & RBF_FLAG_COSINE) ? 1 : 0;
+  const bool fuse = d_idx && score_select_can_merge(e->pitch, k, sh.rows_per_stage, sh.stages, sh.grid);
+  if (fuse) {
+    a.out_idx = d_idx;
+    a.out_score = d_score;
+    a.err_sticky = e->errw + 1;
+    a.result_err = result_err;
+  }
   RBF_LAUNCH(e, launch_score_select(a, e->stream));
   e->last_lists = sh.grid;
   e->last_k = k;
+  if (merged) *merged = fuse;
   return RBF_OK;
 }
 
@@ -614,7 +626,10 @@ rbf_status search_resident_dev(rbf_engine* e, const float* d_query, int32_t k, i
   if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
-  if (rbf_status s = enqueue_score(e, d_query, k)) return s;
+  bool merged = false;
+  if (rbf_status s = enqueue_score(e, d_query, k, d_idx, d_score, reinterpret_cast<int*>(e->result), &merged))
+    return s;
+  if (merged) return RBF_OK;
   return enqueue_merge(e, k, e->last_lists, 1, 0, d_idx, d_score, reinterpret_cast<int*>(e->result));
 }
 
@@ -623,9 +638,13 @@ rbf_status search_resident_dev(rbf_engine* e, const float* d_query, int32_t k, i
 static rbf_status enqueue_host_search(rbf_engine* e, int k, const ResultLayout& L) {
   const size_t qbytes = static_cast<size_t>(e->d) * 4;
   RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
-  if (rbf_status s = enqueue_score(e, e->query, k)) return s;
-  return enqueue_merge(e, k, e->last_lists, 1, 0, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
-                       e->d_hres + L.b_off, reinterpret_cast<int*>(e->d_hres));
+  int32_t* out_idx = reinterpret_cast<int32_t*>(e->d_hres + L.a_off);
+  float* out_score = reinterpret_cast<float*>(e->d_hres + L.b_off);
+  int* result_err = reinterpret_cast<int*>(e->d_hres);
+  bool merged = false;
+  if (rbf_status s = enqueue_score(e, e->query, k, out_idx, out_score, result_err, &merged)) return s;
+  if (merged) return RBF_OK;
+  return enqueue_merge(e, k, e->last_lists, 1, 0, out_idx, out_score, result_err);
 }
 
 // Record enqueue_host_search for this K as a CUDA graph (one launch per

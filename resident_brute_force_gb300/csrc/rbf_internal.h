@@ -48,10 +48,18 @@ struct ScoreSelectLaunch {
   int dynamic;             // 0 = static contiguous row ranges, 1 = tile claims
   uint64_t timeout_ns;
   int normalize_query = 0; // 1: score with the query scaled to unit length (cosine mode)
+  // Set: the last CTA merges the lists into K indices / scores (device or
+  // mapped host memory) and hands the error word to result_err / err_sticky.
+  int32_t* out_idx = nullptr;
+  float* out_score = nullptr;
+  int* err_sticky = nullptr;
+  int* result_err = nullptr;
 };
 
 // Shared memory the fused kernel needs for a launch shape.
 int score_select_smem_bytes(int pitch, int k, int rows_per_stage, int stages);
+// Whether the kernel's ring can hold its last CTA's merge for this shape.
+bool score_select_can_merge(int pitch, int k, int rows_per_stage, int stages, int grid);
 cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream);
 
 struct MergeLaunch {

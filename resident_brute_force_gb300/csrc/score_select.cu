@@ -19,7 +19,12 @@
 //     threshold (its K-th key); rows that beat it are buffered one per lane
 //     and merged 32 at a time;
 //   * at the end the CTA merges its warps' lists in shared memory and writes
-//     one best-first list of KP keys.
+//     one best-first list of KP keys;
+//   * with output pointers, the last CTA to finish (a ticket after a fence)
+//     then merges all the lists itself (section 4 step 4) in the ring's
+//     shared memory and hands over the call's error word, so a search is one
+//     launch; without them the lists are left for the merge kernel.
+#include "merge_core.cuh"
 #include "rbf_device.cuh"
 #include "rbf_internal.h"
 
@@ -28,6 +33,12 @@ namespace {
 
 constexpr int NW = kScoreConsumerWarps;
 constexpr int kThreads = (NW + 1) * 32;
+
+// Keys the fused merge may stage in a ring of `bytes` (the rest holds the
+// survivors).
+__host__ __device__ constexpr int merge_stage_keys(int bytes) {
+  return (bytes / 8 - mergecore::kSurvivorCap - 2) & ~1;
+}
 
 struct Params {
   const float* corpus;
@@ -45,6 +56,12 @@ struct Params {
   int region_bytes;  // ring bytes, or the list scratch if larger
   int dynamic;
   uint64_t timeout_ns;
+  // Merge in the last CTA (when out_idx is set): K indices and scores, and
+  // the per-call error word handed to result_err / err_sticky.
+  int32_t* out_idx;
+  float* out_score;
+  int* err_sticky;
+  int* result_err;
 };
 
 // NCH > 0: rows are exactly NCH * 128 floats and the query lives in
@@ -284,14 +301,42 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
   }
   if (warp == 0) warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
 
-  if (p.dynamic && threadIdx.x == 0) {
-    // The last CTA to finish re-arms the tile counter for the next launch.
-    __threadfence();
+  if (!p.dynamic && !p.out_idx) return;
+  // The last CTA to finish re-arms the tile counter for the next launch and,
+  // when asked, merges every CTA's list.
+  __shared__ int s_last;
+  __threadfence();  // this CTA's list is visible before its ticket
+  __syncthreads();
+  if (threadIdx.x == 0) {
     const unsigned done = atomicAdd(&p.counters[1], 1u);
-    if (done == gridDim.x - 1) {
+    s_last = done == gridDim.x - 1 ? 1 : 0;
+    if (s_last) {
       atomicExch(&p.counters[0], 0u);
       atomicExch(&p.counters[1], 0u);
-      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (s_last && p.out_idx) {
+    __threadfence();
+    mergecore::MergeOut o;
+    o.k = p.k;
+    o.int_keys = 0;
+    o.out_a = p.out_idx;
+    o.out_b = p.out_score;
+    o.kth_out = nullptr;
+    o.q = 0;
+    o.stride = KP;
+    o.lens = nullptr;
+    // The ring only (the barriers after it are left alone).
+    mergecore::merge_lists<KP, kThreads>(o, p.partials, static_cast<int>(gridDim.x), reinterpret_cast<uint64_t*>(smem),
+                                         p.region_bytes, merge_stage_keys(p.region_bytes));
+    if (threadIdx.x == 0) {
+      // Hand the per-call error word to the result block and the sticky
+      // word, then re-arm it for the next call.
+      const int e = atomicOr(p.err, 0);
+      if (p.result_err) *p.result_err = e;
+      if (e && p.err_sticky) atomicOr(p.err_sticky, e);
+      atomicExch(p.err, 0);
     }
   }
 }
@@ -300,10 +345,15 @@ template <int KP, int NCH, bool NORM>
 cudaError_t launch_t(const Params& p, int grid, int smem, cudaStream_t stream) {
   auto fn = score_select_f32_kernel<KP, NCH, NORM>;
   // The launch size depends on the engine's options (at most the device's
-  // opt-in limit), so the limit is raised once to that maximum
-  // (thread-safe static).
-  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                        max_dynamic_smem());
+  // opt-in limit less the kernel's static shared memory), so the limit is
+  // raised once to that maximum (thread-safe static).
+  static const cudaError_t limit = [fn] {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                max_dynamic_smem() - static_cast<int>(fa.sharedSizeBytes));
+  }();
   if (limit != cudaSuccess) return limit;
   fn<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
@@ -332,6 +382,14 @@ int region_bytes(int pitch, int k, int rows_per_stage, int stages) {
 
 }  // namespace
 
+bool score_select_can_merge(int pitch, int k, int rows_per_stage, int stages, int grid) {
+  // The general merge needs a tree of one list per warp plus one staged
+  // list; the fast path applies when its staging fits as well.
+  const int keys = region_bytes(pitch, k, rows_per_stage, stages) / 8;
+  (void)grid;
+  return keys >= (kThreads / 32) * list_width(k) + k;
+}
+
 int score_select_smem_bytes(int pitch, int k, int rows_per_stage, int stages) {
   // region | full[S] empty[S] row0[S] rows[S] (32 B per stage) | query copy
   return region_bytes(pitch, k, rows_per_stage, stages) + stages * 32 + pitch * 4;
@@ -354,6 +412,10 @@ cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream)
   p.region_bytes = region_bytes(a.pitch, a.k, a.rows_per_stage, a.stages);
   p.dynamic = a.dynamic;
   p.timeout_ns = a.timeout_ns;
+  p.out_idx = a.out_idx;
+  p.out_score = a.out_score;
+  p.err_sticky = a.err_sticky;
+  p.result_err = a.result_err;
   const int smem = score_select_smem_bytes(a.pitch, a.k, a.rows_per_stage, a.stages);
   switch (list_width(a.k)) {
     case 32: return launch_kp<32>(p, a.grid, smem, a.normalize_query != 0, stream);
