@@ -1,6 +1,6 @@
 """Small, L2-exceeding cases of each kernel for profiler captures.
 
-    python -m resident_brute_force_gb300.profile_cases single   # scoring + merge, 100k x 1024, K=8
+    python -m resident_brute_force_gb300.profile_cases single   # scoring (+ merge kernel), 100k x 1024, K=8
     python -m resident_brute_force_gb300.profile_cases batch    # batched, 256 queries x 200k x 768, K=32
     python -m resident_brute_force_gb300.profile_cases batch_full  # 256 x 1M x 768, K=8/32/100 (launch lists)
     python -m resident_brute_force_gb300.profile_cases int32    # int32 top-K, 5e7 values, K=20
@@ -32,7 +32,10 @@ def main(part: str) -> None:
         di = torch.empty(256, dtype=torch.int32, device="cuda")
         ds = torch.empty(256, dtype=torch.float32, device="cuda")
         for j in range(4):
-            e.search_resident_dev(dq[j], 8, di, ds)
+            e.search_resident_dev(dq[j], 8, di, ds)  # one launch each (merge in the last CTA)
+        for j in range(3):
+            e.score_select_partials_dev(dq[j], 8)  # the two-step calls: the merge kernel
+            e.merge_partial_topk_dev(8, di, ds)
     elif part == "batch":
         n, d, b = 200_000, 768, 256
         c = workloads.unit_corpus(n, d, seed=1)
