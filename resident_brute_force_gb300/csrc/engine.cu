@@ -712,8 +712,9 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   // The scoring + select kernel over rows [0, rows): one launch per group of
   // up to 256 queries; returns the number of per-CTA lists per query.
   auto score_groups = [&](int64_t rows, int bound_mode, const uint64_t* theta0, int* lists) -> rbf_status {
-    // An even grid for both kernels (the CTA-pair kernel takes 256-row tiles,
-    // so that every query gets the same number of lists).
+    // Clusters of two CTAs over 256-row tiles: an even grid, one list per
+    // query from each CTA of a pair (the CTA holds the query's TMEM lane)
+    // and column half, so grid lists per query.
     const int64_t pair_tiles = (rows + 255) / 256;
     const int grid = 2 * static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pair_tiles, e->num_sms / 2)));
     if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;

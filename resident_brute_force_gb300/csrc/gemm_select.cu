@@ -8,22 +8,20 @@
 // 3-4: per-block partial top-K, then a merge): every CTA leaves one
 // best-first list per query, and the merge kernel finishes each query.
 //
-// Two kernels, one CTA per SM, 10 warps each:
-//   gemm_select_pair_kernel  129-256 queries, every K > 32 and the bound
-//              pre-pass: clusters of two CTAs, tcgen05.mma.cta_group::2 with
-//              M = 256 queries (128 per CTA) and N = 256 corpus rows (128 per
-//              CTA), 6 stages of 32 KB;
-//   gemm_select_kernel       up to 128 queries with K <= 32: one CTA per
-//              128-row tile, M = 128, N = 128, 4 stages of 48 KB.
-// In both:
+// One kernel, gemm_select_pair_kernel: clusters of two CTAs, one CTA per
+// SM, 10 warps each, tcgen05.mma.cta_group::2 with M = 256 queries (128 per
+// CTA) and N = 256 corpus rows (128 per CTA), 6 stages of 32 KB; it serves
+// every batch size and K and the bound pre-pass.
+// Per CTA:
 //   warp 0     TMA producer: per 128-byte K chunk (64 bf16 or 32 fp32
 //              elements) the CTA's queries and corpus rows, 128-byte
 //              swizzled, into the shared-memory ring. The bf16 corpus is
 //              stored tile-major ([row tile][K chunk][128 rows][64]), so each
 //              corpus load is one contiguous 16 KB block of HBM;
-//   warp 1     TMEM owner and MMA issuer: one thread issues the MMAs into one
-//              of two accumulator buffers, so the epilogue drains tile t
-//              while tile t + 1 accumulates;
+//   warp 1     TMEM owner (both CTAs allocate as a pair); in the even CTA
+//              one thread issues the pair's MMAs into one of two
+//              accumulator buffers, so the epilogue drains tile t while
+//              tile t + 1 accumulates;
 //   warps 2-9  epilogue: thread = one query (its TMEM lane) over 128 of the
 //              tile's columns; it marks the scores that may beat its K-th
 //              best, buffers their keys 16 deep in shared memory and merges
@@ -43,13 +41,11 @@
 namespace rbf {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kTileRows = 128;      // corpus rows per tile (MMA N)
 constexpr int kKChunk = 64;         // bf16 elements per 128-byte swizzle row
 constexpr int kKChunkTf32 = 32;     // fp32 (tf32) elements per 128-byte swizzle row
 constexpr int kMmaPerChunk = 4;     // MMAs per 128-byte row: K = 16 bf16 or 8 tf32, 32 bytes each
 constexpr int kSubTileBytes = 128 * kKChunk * 2;  // 16 KB: 128 rows x 128 B
-constexpr int kStageBytes = 3 * kSubTileBytes;    // A0 | A1 | B
 constexpr int kCandCap = 16;        // buffered candidates per query
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
@@ -57,64 +53,8 @@ constexpr int kTmemCols = 512;      // 2 buffers x 2 M tiles x 128 columns
 
 // ------------------------------------------------------------ PTX wrappers
 
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D(tmem) (+)= A(smem) * B(smem)^T, both K-major, fp32 accumulate: bf16
-// operands (kind::f16) or fp32 operands taken as tf32 (kind::tf32).
-template <bool TF32>
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                     uint32_t accumulate) {
-  if constexpr (TF32) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-// Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // 64 consecutive fp32 columns of this thread's TMEM lane, waited for.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -128,26 +68,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Two-dimensional tiled TMA load (x = element offset along the row, y = row).
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
-// Three-dimensional tiled TMA load (x, y within a 16 KB block, z = block).
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -275,9 +195,7 @@ struct Params {
   uint64_t* partials;  // [queries][grid][32] keys; K > 32: [queries][grid][KP], lens[queries][grid] long
   int* err;
   int64_t n;           // corpus rows
-  int num_tiles;       // ceil(n / 128)
   int kchunks;         // 128-byte K chunks per row (64 bf16 or 32 fp32 elements)
-  int num_mt;          // 1 or 2 M tiles of 128 queries in this launch
   int q_row0;          // first query row of this launch in the bf16 query buffer
   int q_count;         // queries in this launch
   int q_out0;          // first query of this launch in the partials layout
@@ -289,274 +207,20 @@ struct Params {
   int wait_inputs;         // 1: the queries come from the kernel launched just before this one
 };
 
-template <int KP, bool TF32>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_select_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
-                       const Params p) {
-  constexpr int CH = Operand<TF32>::kChunk;
-  extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the swizzled tiles.
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);  // [kCandCap][256]
-  uint64_t* full = cand + kCandCap * 256;
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  __shared__ int abort_flag;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4 * p.num_mt);
-    }
-    mbar_init(drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // Launched as a programmatic dependent: the next kernel may be scheduled
-  // now (it waits for this grid before it reads anything written here),
-  // and this one waits for the previous grid before it reads what that
-  // wrote (the queries, the per-query bounds) or writes the lists.
-  pdl_launch_dependents();
-
-  if (warp == 0) {
-    // --------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      if (p.wait_inputs) pdl_wait();
-      const uint64_t pol_c = l2_policy_evict_first();
-      const uint64_t pol_q = l2_policy_evict_last();
-      const uint32_t bytes = static_cast<uint32_t>((p.num_mt + 1) * kSubTileBytes);
-      int64_t it = 0;
-      bool aborted = false;
-      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
-        for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
-          const int s = static_cast<int>(it % kStages);
-          const uint32_t u = static_cast<uint32_t>(it / kStages);
-          if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1u, p.timeout_ns)) {
-            atomicOr(p.err, kErrProducerTimeout);
-            aborted = true;
-            break;
-          }
-          if (*reinterpret_cast<volatile int*>(&abort_flag)) {
-            aborted = true;
-            break;
-          }
-          uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(st, &tmap_q, kc * CH, p.q_row0, &full[s], pol_q);
-          if (p.num_mt > 1) tma_load_2d(st + kSubTileBytes, &tmap_q, kc * CH, p.q_row0 + 128, &full[s], pol_q);
-          if constexpr (TF32)  // the fp32 corpus, row-major
-            tma_load_2d(st + 2 * kSubTileBytes, &tmap_c, kc * CH, t * kTileRows, &full[s], pol_c);
-          else  // the tile-major bf16 copy: one contiguous 16 KB block
-            tma_load_3d(st + 2 * kSubTileBytes, &tmap_c, 0, 0, t * p.kchunks + kc, &full[s], pol_c);
-        }
-      }
-      if (aborted) {
-        abort_flag = 1;
-        // Let every issued load land before the CTA can exit.
-        for (int64_t i = (it > kStages ? it - kStages : 0); i < it; ++i) {
-          const int s = static_cast<int>(i % kStages);
-          if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kStages) & 1u, p.timeout_ns))
-            atomicOr(p.err, kErrDrainTimeout);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(128, kTileRows, Operand<TF32>::kFmt);
-      int64_t it = 0;
-      int tile_i = 0;
-      bool aborted = false;
-      for (int t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x, ++tile_i) {
-        const int b = tile_i & 1;
-        const uint32_t ub = static_cast<uint32_t>(tile_i >> 1);
-        if (ub > 0 && !mbar_wait(&acc_empty[b], (ub - 1) & 1u, p.timeout_ns)) {
-          atomicOr(p.err, kErrConsumerTimeout);
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
-          const int s = static_cast<int>(it % kStages);
-          if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u, p.timeout_ns)) {
-            atomicOr(p.err, kErrConsumerTimeout);
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
-          const uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
-          const uint64_t bdesc = sw128_kmajor_desc(st + 2 * kSubTileBytes);
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            if (m < p.num_mt) {
-              const uint64_t adesc = sw128_kmajor_desc(st + m * kSubTileBytes);
-              const uint32_t d = tmem_base + static_cast<uint32_t>(b * 256 + m * 128);
-#pragma unroll
-              for (int k = 0; k < kMmaPerChunk; ++k) {
-                // Advance both descriptors 32 bytes (16 bf16 or 8 tf32) along K.
-                umma<TF32>(d, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), idesc,
-                           (kc | k) != 0);
-              }
-            }
-          }
-          umma_commit(&empty[s]);  // the stage is free once these MMAs finish
-        }
-        if (aborted) break;
-        umma_commit(&acc_full[b]);  // the accumulator is complete
-      }
-      if (aborted) abort_flag = 1;
-      // Every MMA issued must be finished before TMEM is released.
-      umma_commit(drain);
-      if (!mbar_wait(drain, 0, p.timeout_ns)) atomicOr(p.err, kErrDrainTimeout);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------- epilogue
-    pdl_wait();
-    const int e = warp - 2;
-    const int m = e >> 2;             // M tile
-    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int qlocal = m * 128 + quad * 32 + lane;
-    const int slot = qlocal;          // candidate buffer column
-    uint64_t L[KP];
-#pragma unroll
-    for (int i = 0; i < KP; ++i) L[i] = 0;
-    // theta: every key <= theta is dropped. Without a bound it starts at the
-    // empty key (everything passes until K keys are held). With a bound b on
-    // the final K-th key (the K-th best of a row sample), keys >= b can still
-    // make the top K, so theta starts at b - 1.
-    uint64_t floor_key = 0;
-    if (p.theta0 && qlocal < p.q_count) {
-      const uint64_t b0 = p.theta0[p.q_row0 + qlocal];
-      floor_key = b0 > 0 ? b0 - 1 : 0;
-    }
-    uint64_t theta = floor_key;
-    float theta_f = floor_key ? key_score(floor_key + 1) : 0.0f;
-    bool filling = floor_key == 0;
-    int cnt = 0;
-
-    // Merge every buffered candidate into the list, 8 at a time, for as many
-    // batches as the fullest lane of the warp needs.
-    auto merge_buffer = [&]() {
-      const int batches = static_cast<int>((__reduce_max_sync(kFullMask, static_cast<unsigned>(cnt)) + 7u) >> 3);
-#pragma unroll 1
-      for (int b8 = 0; b8 < batches * 8; b8 += 8) {
-        uint64_t c[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = (b8 + i < cnt) ? cand[(b8 + i) * 256 + slot] : 0ull;
-        sort_desc(c);
-        list_merge8<KP>(L, c);
-      }
-      cnt = 0;
-      theta = umax64(list_get<KP>(L, p.k - 1), floor_key);
-      filling = theta == 0;
-      theta_f = filling ? 0.0f : key_score(theta == floor_key ? floor_key + 1 : theta);
-    };
-
-    if (m < p.num_mt) {
-      int tile_i = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
-        const int b = tile_i & 1;
-        if (!__all_sync(kFullMask, mbar_wait(&acc_full[b], static_cast<uint32_t>(tile_i >> 1) & 1u, p.timeout_ns))) {
-          if (lane == 0) atomicOr(p.err, kErrConsumerTimeout);
-          abort_flag = 1;
-          break;
-        }
-        if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) break;
-        tc_fence_after();
-        const int64_t row0 = static_cast<int64_t>(t) * kTileRows;
-        // Two 64-column TMEM loads per tile; the accumulator buffer is handed
-        // back to the MMA warp as soon as the second one has landed, before
-        // its columns are examined.
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(b * 256 + m * 128);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float s64[64];
-          tmem_ld64(tbase + static_cast<uint32_t>(h * 64), s64);
-          if (h == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[b]);
-          }
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const float(&sc)[32] = *reinterpret_cast<const float(*)[32]>(&s64[c2 * 32]);
-            const int64_t rb = row0 + h * 64 + c2 * 32;
-            // One bit per column whose score may beat theta (a superset test:
-            // ties are settled below by the key compare), built without
-            // branches; rows past the corpus end are masked off.
-            uint32_t m = 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) m |= (sc[j] >= theta_f) ? (1u << j) : 0u;
-            if (filling) m = 0xFFFFFFFFu;
-            if (p.n - rb < 32) m &= (p.n - rb > 0) ? ((1u << (p.n - rb)) - 1u) : 0u;
-            // Walk the columns any lane flagged, in order, warp-uniformly.
-            uint32_t u = __reduce_or_sync(kFullMask, m);
-            while (u) {
-              const int j = __ffs(u) - 1;
-              u &= u - 1;
-              if (m & (1u << j)) {
-                const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j));
-                if (key > theta) {
-                  cand[cnt * 256 + slot] = key;
-                  ++cnt;
-                }
-              }
-              if (__any_sync(kFullMask, cnt == kCandCap)) merge_buffer();
-            }
-          }
-        }
-      }
-      if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
-      // Every MMA has finished (the last accumulator was full), so the ring
-      // is free for the transposed list write.
-      uint64_t* dst = qlocal < p.q_count
-                          ? p.partials + (static_cast<size_t>(p.q_out0 + qlocal) * gridDim.x + blockIdx.x) * 32
-                          : nullptr;
-      store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane, dst,
-                    [&](int i) { return i < KP ? L[i] : 0ull; });
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
-}
-
-// ------------------------------------------------ CTA-pair variant (2 SMs)
+// ------------------------------------------------ CTA pairs (2 SMs)
 //
-// For 129-256 queries. A cluster of two CTAs computes each 256-row corpus tile
-// against all 256 queries with tcgen05.mma.cta_group::2 (M = 256, N = 256,
-// K = 16). Per 64-wide K chunk each CTA stages only its own 128 queries (A)
-// and 128 of the tile's rows (B), 32 KB, so six stages fit; the MMA reads
-// both CTAs' shared memory and writes each CTA's TMEM (its 128 queries x 256
-// rows). The even CTA of the pair issues the MMAs and multicasts each commit
-// to both CTAs' barriers; the odd CTA's loads complete on the even CTA's full
+// A cluster of two CTAs computes each 256-row corpus tile against up to 256
+// queries with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16). Per
+// 128-byte K chunk each CTA stages only its own 128 queries (A) and 128 of
+// the tile's rows (B), 32 KB, so six stages fit; the MMA reads both CTAs'
+// shared memory and writes each CTA's TMEM (its 128 queries x 256 rows). The
+// even CTA of the pair issues the MMAs and multicasts each commit to both
+// CTAs' barriers; the odd CTA's loads complete on the even CTA's full
 // barrier, and both CTAs' epilogues release an accumulator on the even CTA's
-// barrier. Per SM and stage this moves 2/3 of the bytes of the single-CTA
-// kernel for the same tensor work.
+// barrier. Lanes past the batch (up to 128 queries: the odd CTA's, and the
+// padding of a partial group) mark nothing. (A single-CTA variant with two
+// M tiles per CTA moved 1.5x the bytes per SM and stage for the same tensor
+// work and could not cover a stage's round trip with four 48 KB stages.)
 
 constexpr int kPairStages = 6;
 constexpr int kPairStageBytes = 2 * kSubTileBytes;  // A (own 128 queries) | B (own 128 rows)
@@ -686,10 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Programmatic dependent launch, as in gemm_select_kernel: the corpus
-  // stream starts while the previous kernel finishes unless that kernel
-  // wrote the queries; the epilogue waits for it before it reads the bounds
-  // or writes any list.
+  // Launched as a programmatic dependent: the next kernel may be scheduled
+  // now (it waits for this grid before it reads anything written here). The
+  // corpus stream starts while the previous kernel finishes unless that
+  // kernel wrote the queries; the epilogue waits for it before it reads the
+  // bounds or writes any list.
   pdl_launch_dependents();
 
   if (warp == 0) {
@@ -1008,27 +673,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int KP, bool TF32>
-cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
-  auto fn = gemm_select_kernel<KP, TF32>;
-  const int smem = gemm_select_smem_bytes();
-  // Set once per instance (a function-local static is initialised once, even
-  // with callers on several host threads).
-  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (limit != cudaSuccess) return limit;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fn, tq, tc, p);
-}
-
 int pair_smem_bytes() {
   return 1024 + kPairStages * kPairStageBytes + kCandCap * 256 * 8 + (2 * kPairStages + 5) * 8 + 16;
 }
@@ -1090,10 +734,6 @@ __global__ void to_bf16_tiled_kernel(const float* __restrict__ src, int64_t src_
 }
 
 }  // namespace
-
-int gemm_select_smem_bytes() {
-  return 1024 + kStages * kStageBytes + kCandCap * 256 * 8 + (2 * kStages + 5) * 8 + 16;
-}
 
 bool make_bf16_tensor_map(void* map_out, const void* base, int64_t rows, int pitch_elems) {
   CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
@@ -1166,7 +806,7 @@ cudaError_t launch_typed(const CUtensorMap& tq, const CUtensorMap& tc, const Par
   if (a.grid < 2 || a.grid % 2 != 0) return cudaErrorInvalidValue;
   if (a.bound_mode) return launch_pair_t<8, TF32>(tq, tc, p, a.grid, stream);
   if (a.k > 32) {
-    // Lists in global memory, any number of queries: CTA pairs.
+    // Lists in global memory.
     if (!a.lens) return cudaErrorInvalidValue;
     // List stride list_width(K), as the merge reads it.
     if (a.k <= 64) return launch_pair_t<64, TF32>(tq, tc, p, a.grid, stream);
@@ -1174,16 +814,10 @@ cudaError_t launch_typed(const CUtensorMap& tq, const CUtensorMap& tc, const Par
     if (a.k <= 256) return launch_pair_t<256, TF32>(tq, tc, p, a.grid, stream);
     return cudaErrorInvalidValue;
   }
-  if (a.q_count > 128) {
-    // Two M tiles: a CTA pair per 256-row tile (lists per query = grid).
-    if (a.k <= 8) return launch_pair_t<8, TF32>(tq, tc, p, a.grid, stream);
-    if (a.k <= 16) return launch_pair_t<16, TF32>(tq, tc, p, a.grid, stream);
-    if (a.k <= 32) return launch_pair_t<32, TF32>(tq, tc, p, a.grid, stream);
-    return cudaErrorInvalidValue;
-  }
-  if (a.k <= 8) return launch_t<8, TF32>(tq, tc, p, a.grid, stream);
-  if (a.k <= 16) return launch_t<16, TF32>(tq, tc, p, a.grid, stream);
-  if (a.k <= 32) return launch_t<32, TF32>(tq, tc, p, a.grid, stream);
+  // Register lists (lists per query = grid), any number of queries up to 256.
+  if (a.k <= 8) return launch_pair_t<8, TF32>(tq, tc, p, a.grid, stream);
+  if (a.k <= 16) return launch_pair_t<16, TF32>(tq, tc, p, a.grid, stream);
+  if (a.k <= 32) return launch_pair_t<32, TF32>(tq, tc, p, a.grid, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -1192,9 +826,7 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.partials = a.partials;
   p.err = a.err;
   p.n = a.n;
-  p.num_tiles = static_cast<int>((a.n + kTileRows - 1) / kTileRows);
   p.kchunks = a.kchunks;
-  p.num_mt = a.q_count > 128 ? 2 : 1;
   p.q_row0 = a.q_row0;
   p.q_count = a.q_count;
   p.q_out0 = a.q_out0;

@@ -150,7 +150,6 @@ struct GemmSelectLaunch {
   int wait_inputs = 1;       // 1: the kernel launched just before wrote the queries (the producer waits
                              // for it); 0: the corpus stream may start while that kernel finishes
 };
-int gemm_select_smem_bytes();
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
 bool make_bf16_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);
 // Tensor map over a [rows][pitch] fp32 matrix: 32 x 128 boxes, 128-byte swizzle
