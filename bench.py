@@ -291,6 +291,10 @@ def run_batched(rbf, steps, warmup, tf32=False):
         dik = torch.empty((b, kk), dtype=torch.int32, device="cuda")
         dsk = torch.empty((b, kk), dtype=torch.float32, device="cuda")
         other[kk] = time_device(st, lambda: e.search_resident_batch_dev(dq, kk, dik, dsk), steps, warmup)
+    # A small batch (16 queries, K = 32): the same corpus pass for fewer queries.
+    di16 = torch.empty((16, k), dtype=torch.int32, device="cuda")
+    ds16 = torch.empty((16, k), dtype=torch.float32, device="cuda")
+    ms16 = time_device(st, lambda: e.search_resident_batch_dev(dq[:16], k, di16, ds16), steps, warmup)
     e.close()
     p50 = percentile(ms, 50) * 1e-3
     flops = 2.0 * b * n * d
@@ -312,6 +316,7 @@ def run_batched(rbf, steps, warmup, tf32=False):
             "queries_per_s": round(b / p50, 1),
             "k8_p50_us": round(percentile(other[8], 50) * 1e3, 1),
             "k100_p50_us": round(percentile(other[100], 50) * 1e3, 1),
+            "b16_p50_us": round(percentile(ms16, 50) * 1e3, 1),
             "launches_per_call": 5, "steps": len(ms)}
 
 
