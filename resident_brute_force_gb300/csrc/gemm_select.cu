@@ -593,11 +593,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t rb = row0 + hh * 64 + c2 * 32;
           if constexpr (KP == 8) {
             if (bound) {
-              uint64_t top = 0;
+              // The chunk's best key: its largest score (NaN ignored) at the
+              // first column holding it, one key built per chunk. Any row's
+              // key of the chunk would keep the bound valid (K chunks give K
+              // distinct rows); all-NaN chunks take their first row.
+              const int64_t left = p.n - rb;
+              const int nvalid = left >= 32 ? 32 : (left > 0 ? static_cast<int>(left) : 0);
+              if (nvalid > 0) {
+                float t16[16];
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                top = umax64(top, (rb + j < p.n) ? make_key(sc[j], static_cast<uint32_t>(rb + j)) : 0ull);
-              best[hh * 2 + c2] = umax64(best[hh * 2 + c2], top);
+                for (int j = 0; j < 16; ++j)
+                  t16[j] = fmaxf(j < nvalid ? sc[j] : -INFINITY, j + 16 < nvalid ? sc[j + 16] : -INFINITY);
+#pragma unroll
+                for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                  for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
+                const float mx = t16[0];
+                uint32_t eq = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) eq |= (j < nvalid && sc[j] == mx) ? (1u << j) : 0u;
+                const int jm = eq ? __ffs(eq) - 1 : 0;
+                best[hh * 2 + c2] = umax64(best[hh * 2 + c2], make_key(mx, static_cast<uint32_t>(rb + jm)));
+              }
               continue;
             }
           }
