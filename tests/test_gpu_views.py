@@ -151,3 +151,60 @@ def test_upload_on_base_reaches_views_and_rules(rbf):
     finally:
         v.close()
         base.close()
+
+
+def test_concurrent_batched_and_int32_on_views(rbf):
+    """Batched searches (K = 32 and K = 100, the latter through per-thread lists in each handle's
+    own partials buffer) and int32 top-K calls issued on three handles' streams without
+    synchronisation in between: every result equals the one computed alone."""
+    import torch
+    n, d, b = 70_144, 128, 40
+    c = workloads.dyadic_grid(n, d, seed=91)
+    qs = workloads.dyadic_grid(3 * b, d, seed=92)
+    x = torch.from_numpy(workloads.int32_uniform(2_000_000, seed=93)).cuda()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    base = rbf.Engine(n, d, 128, max_batch=b, flags=rbf.RBF_FLAG_BF16_CORPUS, stream=streams[0])
+    base.upload_corpus_rowmajor(c)
+    hs = [base] + [base.view(stream=s) for s in streams[1:]]
+    try:
+        dq = torch.from_numpy(qs).cuda()
+        jobs = [(32, 0), (100, 1), (32, 2)]
+        ref = []
+        for k, part in jobs:
+            di = torch.empty((b, k), dtype=torch.int32, device="cuda")
+            ds = torch.empty((b, k), dtype=torch.float32, device="cuda")
+            base.search_resident_batch_dev(dq[part * b:(part + 1) * b], k, di, ds)
+            torch.cuda.synchronize()
+            ref.append((di.clone(), ds.clone()))
+        dv_ref = torch.empty(50, dtype=torch.int32, device="cuda")
+        dp_ref = torch.empty(50, dtype=torch.int64, device="cuda")
+        base.topk_int32_dev(x, 50, dv_ref, dp_ref)
+        torch.cuda.synchronize()
+        for rep in range(3):
+            outs = []
+            for h, s, (k, part) in zip(hs, streams, jobs):
+                di = torch.zeros((b, k), dtype=torch.int32, device="cuda")
+                ds = torch.zeros((b, k), dtype=torch.float32, device="cuda")
+                dv = torch.zeros(50, dtype=torch.int32, device="cuda")
+                dp = torch.zeros(50, dtype=torch.int64, device="cuda")
+                torch.cuda.synchronize()
+                outs.append((di, ds, dv, dp))
+            for h, s, (k, part), (di, ds, dv, dp) in zip(hs, streams, jobs, outs):
+                with torch.cuda.stream(s):
+                    h.search_resident_batch_dev(dq[part * b:(part + 1) * b], k, di, ds)
+                    h.topk_int32_dev(x, 50, dv, dp)
+            torch.cuda.synchronize()
+            for j, (di, ds, dv, dp) in enumerate(outs):
+                assert torch.equal(di, ref[j][0]) and torch.equal(ds, ref[j][1]), (rep, j)
+                assert torch.equal(dv, dv_ref) and torch.equal(dp, dp_ref), (rep, j)
+        for j, (k, part) in enumerate(jobs):
+            for q in range(0, b, 13):
+                idx = ref[j][0][q].cpu().numpy()
+                sc = ref[j][1][q].cpu().numpy()
+                check_exact(idx, sc, *oracle.topk(c, qs[part * b + q], k))
+        for h in hs:
+            assert h.check_device_error() == rbf.RBF_OK
+    finally:
+        for h in hs[1:]:
+            h.close()
+        base.close()
