@@ -277,7 +277,11 @@ rbf_status rbf_selftest_wait_timeout(rbf_engine* engine, uint64_t timeout_ns);
 
 /* Host-side fault injection for tests: the next `count` CUDA operations of the
  * given kind report failure without being issued. kind: 1 = copy, 2 = kernel
- * launch. count 0 clears. Touches no GPU state. */
+ * launch. count 0 clears. Touches no GPU state. Allocation failures are
+ * injected through the environment instead (there is no engine yet): with
+ * RBF_FAULT=alloc set, rbf_create and rbf_create_view fail with
+ * RBF_ERR_OUT_OF_MEMORY as if a device allocation had failed, after freeing
+ * what they had allocated. */
 rbf_status rbf_inject_host_fault(rbf_engine* engine, int32_t kind, int32_t count);
 
 #ifdef __cplusplus

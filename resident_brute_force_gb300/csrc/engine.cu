@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -299,10 +300,17 @@ void release(rbf_engine* e) {
   delete e;
 }
 
+// RBF_FAULT=alloc: make the engine's allocations fail (tests of the
+// out-of-memory path; nothing is issued to the GPU for it).
+bool alloc_fault_armed() {
+  const char* v = std::getenv("RBF_FAULT");
+  return v && std::strcmp(v, "alloc") == 0;
+}
+
 // Every per-call buffer of an engine or a view (not the corpus). On failure
 // the engine is released.
 rbf_status alloc_call_buffers(rbf_engine* e) {
-  bool ok = true;
+  bool ok = !alloc_fault_armed();
   if (e->flags & RBF_FLAG_BF16_CORPUS)
     ok = ok && cudaMalloc(&e->query_bf16, static_cast<size_t>(e->query_rows) * e->max_pitch_bf16 * 2) == cudaSuccess;
   else
@@ -439,7 +447,7 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   const size_t result_count = static_cast<size_t>(max_batch) * max_k;
   e->result_bytes = result_layout(result_count, 8).bytes;
 
-  bool ok = true;
+  bool ok = !alloc_fault_armed();
   if (flags & RBF_FLAG_FP32_CORPUS)
     ok = ok && cudaMalloc(&e->corpus, static_cast<size_t>(max_n) * e->max_pitch * sizeof(float)) == cudaSuccess;
   if (flags & RBF_FLAG_BF16_CORPUS)

@@ -271,3 +271,50 @@ def test_full_size_planted(rbf):
                 idx, sc = e.search_resident(qs[j], k)
                 check_float_topk(idx, sc, sigma, k)
         del torch
+
+
+def test_out_of_memory_paths(rbf, monkeypatch):
+    """rbf_create reports RBF_ERR_OUT_OF_MEMORY and leaks nothing: for a real
+    over-size request (64 TB of corpus) and for an injected allocation
+    failure (RBF_FAULT=alloc), for engines and views; afterwards engines work."""
+    with pytest.raises(rbf.RbfError) as ei:
+        rbf.Engine(2**31 - 1, 8192, 8)
+    assert ei.value.status == rbf.RBF_ERR_OUT_OF_MEMORY
+    c = workloads.dyadic_grid(500, 32, seed=73)
+    base = rbf.Engine(500, 32, 8)
+    try:
+        base.upload_corpus_rowmajor(c)
+        monkeypatch.setenv("RBF_FAULT", "alloc")
+        for make in (lambda: rbf.Engine(500, 32, 8), lambda: base.view()):
+            with pytest.raises(rbf.RbfError) as ei:
+                make()
+            assert ei.value.status == rbf.RBF_ERR_OUT_OF_MEMORY
+        monkeypatch.delenv("RBF_FAULT")
+        with base.view() as v:
+            check_exact(*v.search_resident(c[7], 8), *oracle.topk(c, c[7], 8))
+    finally:
+        base.close()
+
+
+def test_repeated_calls_are_bit_identical(rbf):
+    """The same query 100 times (single query, batched and int32): every result
+    is the same bytes, so no ordering inside a kernel leaks into the output."""
+    import torch
+    n, d = 30_000, 256
+    c = workloads.unit_corpus(n, d, seed=74)
+    qs = workloads.unit_queries(16, d, seed=75)
+    x = torch.from_numpy(workloads.int32_uniform(1_000_000, seed=76)).cuda()
+    with rbf.Engine(n, d, 100, max_batch=16, flags=rbf.RBF_FLAG_BF16_CORPUS) as e:
+        e.upload_corpus_rowmajor(c)
+        first = e.search_resident(qs[0], 100)
+        first_b = e.search_resident_batch(qs, 100)
+        first_i = e.topk_int32(x, 64)
+        for _ in range(100):
+            idx, sc = e.search_resident(qs[0], 100)
+            assert np.array_equal(idx, first[0]) and np.array_equal(sc, first[1])
+        for _ in range(100):
+            idx, sc = e.search_resident_batch(qs, 100)
+            assert np.array_equal(idx, first_b[0]) and np.array_equal(sc, first_b[1])
+            v, p = e.topk_int32(x, 64)
+            assert np.array_equal(v, first_i[0]) and np.array_equal(p, first_i[1])
+        check_float_topk(first[0], first[1], oracle.scores(c, qs[0]), 100)
