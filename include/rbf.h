@@ -48,7 +48,9 @@ typedef enum rbf_status {
   RBF_ERR_OUT_OF_MEMORY = 3, /* rbf_create could not allocate */
   RBF_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   RBF_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
-  RBF_ERR_UNSUPPORTED = 6    /* valid request this build does not handle */
+  RBF_ERR_UNSUPPORTED = 6,   /* valid request this build does not handle */
+  RBF_ERR_BOUNDS = 7         /* checked builds (RBF_CHECKS) only: a kernel met an index outside
+                                its buffer and skipped the access; the outputs are not valid */
 } rbf_status;
 
 /* Largest K any entry point accepts (the article's kMaxSupportedK,
@@ -144,7 +146,8 @@ const char* rbf_status_string(rbf_status status);
 int32_t rbf_last_cuda_error(const rbf_engine* engine);
 
 /* Synchronise the stream and return (and clear) any error a device kernel
- * recorded since the last check: RBF_ERR_TIMEOUT if a bounded wait ran out. */
+ * recorded since the last check: RBF_ERR_TIMEOUT if a bounded wait ran out,
+ * RBF_ERR_BOUNDS if a checked build skipped an access outside its buffer. */
 rbf_status rbf_check_device_error(rbf_engine* engine);
 
 /* ------------------------------------------------------------------ ingest */

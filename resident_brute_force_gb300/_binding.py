@@ -21,6 +21,7 @@ RBF_ERR_OUT_OF_MEMORY = 3
 RBF_ERR_CUDA = 4
 RBF_ERR_TIMEOUT = 5
 RBF_ERR_UNSUPPORTED = 6
+RBF_ERR_BOUNDS = 7
 
 RBF_MAX_K = 256
 RBF_MAX_D = 8192
@@ -74,7 +75,9 @@ _lib = None
 
 
 def lib_path() -> str:
-    return _build.LIB_PATH
+    """The library to load: RBF_LIB if set (e.g. the checked build), else the
+    in-tree librbf.so."""
+    return os.environ.get("RBF_LIB") or _build.LIB_PATH
 
 
 def load_library(path: str | None = None) -> ctypes.CDLL:

@@ -17,6 +17,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "librbf.so")
+# The checked variant (-DRBF_CHECKS: device-side bounds checks on the indices
+# the kernels derive, reported through the error word).
+CHECKS_BUILD_DIR = os.path.join(HERE, "_build_checks")
+CHECKS_LIB_PATH = os.path.join(HERE, "librbf_checks.so")
 
 SOURCES = ["engine.cu", "score_select.cu", "merge.cu", "topk_i32.cu", "noalloc.cu", "gemm_select.cu", "normalize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -36,23 +40,27 @@ def _deps() -> list[str]:
     return files
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Build librbf.so if any source is newer than it (or ``force``)."""
-    if not force and not is_stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          checks: bool = False) -> str:
+    """Build librbf.so (or, with ``checks``, librbf_checks.so) if any source is
+    newer than it (or ``force``)."""
+    lib = CHECKS_LIB_PATH if checks else LIB_PATH
+    build_dir = CHECKS_BUILD_DIR if checks else BUILD_DIR
+    if not force and not is_stale(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DRBF_CHECKS"] if checks else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,10 +71,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib

@@ -18,6 +18,7 @@
 #include <new>
 
 #include "../../include/rbf.h"
+#include "rbf_device.cuh"
 #include "rbf_internal.h"
 
 using namespace rbf;
@@ -132,6 +133,18 @@ bool inject(rbf_engine* e, int kind) {
   return false;
 }
 
+// The partials capacity the kernels check their list slots against (checked
+// builds). There RBF_FAULT=bounds understates it, so that the checks fire --
+// the accesses are skipped and the bounds bit set -- without any access
+// outside the buffer.
+size_t device_cap(const rbf_engine* e) {
+#ifdef RBF_CHECKS
+  const char* v = std::getenv("RBF_FAULT");
+  if (v && std::strcmp(v, "bounds") == 0) return 64;
+#endif
+  return e->partials_cap;
+}
+
 #define RBF_COPY(e, call)                              \
   do {                                                 \
     if (inject((e), 1)) return RBF_ERR_CUDA;           \
@@ -207,6 +220,7 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_
   a.grid = sh.grid;
   a.dynamic = e->dynamic;
   a.timeout_ns = e->timeout_ns;
+  a.partials_cap = device_cap(e);
   // Cosine mode: rows are unit length already; the kernel scales its copy of
   // the query to unit length, so the inner product is the cosine.
   a.normalize_query = (e->flags & RBF_FLAG_COSINE) ? 1 : 0;
@@ -237,6 +251,7 @@ rbf_status enqueue_merge(rbf_engine* e, int k, int lists, int queries, int int_k
   m.err_call = e->errw;
   m.err_sticky = e->errw + 1;
   m.result_err = result_err;
+  m.partials_cap = device_cap(e);
   RBF_LAUNCH(e, launch_merge(m, e->stream));
   return RBF_OK;
 }
@@ -263,6 +278,7 @@ rbf_status finish_host_call(rbf_engine* e, const ResultLayout& L) {
   if (st != cudaSuccess) return cuda_fail(e, st);
   int derr = 0;
   std::memcpy(&derr, e->h_result, sizeof(int));
+  if (derr & kErrBounds) return RBF_ERR_BOUNDS;
   if (derr != 0) return RBF_ERR_TIMEOUT;
   return RBF_OK;
 }
@@ -388,6 +404,7 @@ const char* rbf_status_string(rbf_status s) {
     case RBF_ERR_CUDA: return "RBF_ERR_CUDA";
     case RBF_ERR_TIMEOUT: return "RBF_ERR_TIMEOUT";
     case RBF_ERR_UNSUPPORTED: return "RBF_ERR_UNSUPPORTED";
+    case RBF_ERR_BOUNDS: return "RBF_ERR_BOUNDS";
   }
   return "RBF_ERR_UNKNOWN";
 }
@@ -562,6 +579,7 @@ rbf_status rbf_check_device_error(rbf_engine* e) {
   if (st == cudaSuccess) st = cudaMemsetAsync(e->errw + 1, 0, sizeof(int), e->stream);
   if (st == cudaSuccess) st = cudaStreamSynchronize(e->stream);
   if (st != cudaSuccess) return cuda_fail(e, st);
+  if (w & kErrBounds) return RBF_ERR_BOUNDS;
   return w ? RBF_ERR_TIMEOUT : RBF_OK;
 }
 
@@ -743,6 +761,9 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
       a.timeout_ns = e->timeout_ns;
       a.theta0 = theta0;
       a.bound_mode = bound_mode;
+      a.partials_cap = device_cap(e);
+      a.lens_cap = static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms;
+      a.theta_cap = static_cast<size_t>(e->max_batch);
       // Only the first launch after the query staging waits for it before
       // streaming (after the bound merge, or another group, the queries are
       // long complete).
@@ -779,6 +800,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     m.err_call = nullptr;
     m.err_sticky = nullptr;
     m.result_err = nullptr;
+    m.partials_cap = device_cap(e);
     m.kth_out = e->theta0;
     m.stride = kBatchListWidth;
     m.short_lists = k > kBatchRegMaxK ? 1 : 0;  // 4 chunk maxima per list
@@ -817,6 +839,9 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     a.timeout_ns = e->timeout_ns;
     a.theta0 = theta0;
     a.lens = e->lens;
+    a.partials_cap = device_cap(e);
+    a.lens_cap = static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms;
+    a.theta_cap = static_cast<size_t>(e->max_batch);
     a.wait_inputs = (q0 == 0 && theta0 == nullptr) ? 1 : 0;
     RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
     MergeLaunch m;
@@ -830,6 +855,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     m.err_call = last ? e->errw : nullptr;
     m.err_sticky = e->errw + 1;
     m.result_err = last ? result_err : nullptr;
+    m.partials_cap = device_cap(e);
     m.stride = kw;
     m.lens = e->lens;
     m.short_lists = 1;
@@ -881,6 +907,8 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
     a.n = count;
     a.k = k;
     a.partials = e->partials;
+    a.partials_cap = device_cap(e);
+    a.err = e->errw;
     a.grid = static_cast<int>(grid);
     RBF_LAUNCH(e, launch_topk_i32_stage1(a, e->stream));
     *lists = static_cast<int>(grid);
@@ -912,6 +940,7 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
     m.err_call = nullptr;
     m.err_sticky = nullptr;
     m.result_err = nullptr;
+    m.partials_cap = device_cap(e);
     m.kth_out = e->i32_theta0;
     RBF_LAUNCH(e, launch_merge(m, e->stream));
     theta0 = e->i32_theta0;
@@ -921,6 +950,7 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
   a.n = n;
   a.k = k;
   a.partials = e->partials;
+  a.partials_cap = device_cap(e);
   a.theta0 = theta0;
   a.counters = e->counters + 2;
   a.err = e->errw;

@@ -205,6 +205,9 @@ struct Params {
   int bound_mode;          // 1 (CTA pairs, KP = 8): write 4 chunk maxima per list instead of a top-K list
   int* lens;               // K > 32: valid keys of each list
   int wait_inputs;         // 1: the queries come from the kernel launched just before this one
+  size_t partials_cap;     // keys, lens entries and theta0 entries, for checked builds
+  size_t lens_cap;         // (0: not checked)
+  size_t theta_cap;
 };
 
 // ------------------------------------------------ CTA pairs (2 SMs)
@@ -470,10 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t L[kWide ? 1 : KP];
 #pragma unroll
     for (int i = 0; i < (kWide ? 1 : KP); ++i) L[i] = 0;
-    const bool live = qidx < p.q_count;
     auto list_id = [&]() {
       return static_cast<size_t>(p.q_out0 + qidx) * gridDim.x + static_cast<size_t>(cluster * 2 + h);
     };
+    // A lane past the batch, or (checked builds) one whose list would fall
+    // outside the buffers, marks nothing and writes nothing.
+    const bool live =
+        qidx < p.q_count &&
+        in_bounds(p.partials_cap == 0 || (list_id() + 1) * (kWide ? KP : 32) <= p.partials_cap, p.err) &&
+        in_bounds(!kWide || p.lens_cap == 0 || list_id() < p.lens_cap, p.err) &&
+        in_bounds(!p.theta0 || p.theta_cap == 0 || static_cast<size_t>(p.q_row0 + qidx) < p.theta_cap, p.err);
     uint64_t* lst = nullptr;
     if constexpr (kWide) lst = p.partials + list_id() * KP;
     int len = 0;
@@ -853,6 +862,9 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.bound_mode = a.bound_mode;
   p.lens = a.lens;
   p.wait_inputs = a.wait_inputs;
+  p.partials_cap = a.partials_cap;
+  p.lens_cap = a.lens_cap;
+  p.theta_cap = a.theta_cap;
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
   return a.tf32 ? launch_typed<true>(tq, tc, p, a, stream) : launch_typed<false>(tq, tc, p, a, stream);

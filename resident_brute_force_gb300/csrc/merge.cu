@@ -34,6 +34,7 @@ struct Params {
   int stride;         // keys from one list to the next
   const int* lens;    // optional: [query][list] valid keys per list
   int stage_keys;     // shared-memory budget (keys) for staged list heads
+  size_t partials_cap;  // keys (checked builds; 0: not checked)
 };
 
 constexpr int kManyQueries = 64;          // from this many queries on, merge CTAs are 8 warps
@@ -55,6 +56,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
   o.q = blockIdx.x;
   o.stride = p.stride;
   o.lens = p.lens ? p.lens + static_cast<size_t>(blockIdx.x) * p.lists : nullptr;
+  if (p.partials_cap) {
+    const size_t off = static_cast<size_t>(blockIdx.x) * p.lists * p.stride;
+    o.region = p.partials_cap > off ? p.partials_cap - off : 1;  // 1: every read is out of bounds
+  }
+  o.err = p.err_sticky ? p.err_sticky : p.err_call;
   mergecore::merge_lists<KP, WARPS * 32>(o, base, p.lists, smem, p.smem_bytes, p.stage_keys);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.err_call) {
     // Hand the per-call device error word to the host-visible result and
@@ -106,6 +112,7 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.kth_out = a.kth_out;
   p.stride = a.stride > 0 ? a.stride : list_width(a.k);
   p.lens = a.lens;
+  p.partials_cap = a.partials_cap;
   // Short lists (a prefix of K valid keys, or fewer): stage 32 keys of each
   // (the rest is read from L2 if it survives), so that the CTA's shared
   // memory stays small and all queries run in one wave.

@@ -49,6 +49,8 @@ struct MergeOut {
   size_t q;
   int stride;
   const int* lens;
+  size_t region = 0;  // keys readable from the lists' base (checked builds; 0: not checked)
+  int* err = nullptr; // where a checked build reports an index outside region
 };
 
 // Valid keys of list l.
@@ -56,7 +58,8 @@ __device__ __forceinline__ int list_len(const MergeOut& p, int l) { return p.len
 
 // Key e of list l, or the empty key past the list's end.
 __device__ __forceinline__ uint64_t list_key(const MergeOut& p, const uint64_t* base, int l, int e) {
-  return e < list_len(p, l) ? __ldcg(base + static_cast<size_t>(l) * p.stride + e) : 0ull;
+  const size_t off = static_cast<size_t>(l) * p.stride + e;
+  return e < list_len(p, l) && in_bounds(p.region == 0 || off < p.region, p.err) ? __ldcg(base + off) : 0ull;
 }
 
 constexpr int kSurvivorCap = 2048;  // keys gathered by the fast path

@@ -89,6 +89,7 @@ extern "C" rbf_status topk_int32_noalloc(const int32_t* d_data, int64_t n, int32
   a.n = n;
   a.k = k;
   a.partials = s.lists;  // every list is written in full before it is read
+  a.partials_cap = static_cast<size_t>(kNoallocMaxLists) * kNoallocListWidth;
   a.grid = static_cast<int>(grid);
   if (launch_topk_i32_stage1(a, stream) != cudaSuccess) return RBF_ERR_CUDA;
 
@@ -103,6 +104,7 @@ extern "C" rbf_status topk_int32_noalloc(const int32_t* d_data, int64_t n, int32
   m.err_call = nullptr;  // these kernels never wait, so there is no device error word
   m.err_sticky = nullptr;
   m.result_err = nullptr;
+  m.partials_cap = static_cast<size_t>(kNoallocMaxLists) * kNoallocListWidth;
   if (launch_merge(m, stream) != cudaSuccess) return RBF_ERR_CUDA;
   return RBF_OK;
 }

@@ -22,6 +22,21 @@ constexpr int kErrConsumerTimeout = 1;
 constexpr int kErrProducerTimeout = 2;
 constexpr int kErrDrainTimeout = 4;
 constexpr int kErrProbeTimeout = 8;
+constexpr int kErrBounds = 16;  // a checked build met an index outside its buffer
+
+// Checked builds (-DRBF_CHECKS): true when the access may go ahead; else the
+// bounds bit is ORed into the error word and the caller skips the access.
+// Other builds compile the check away. Used on the indices the kernels derive
+// (list slots, list lengths, per-query offsets), not on the bulk and tensor
+// copies, whose extents come straight from N and the tile sizes.
+#ifdef RBF_CHECKS
+__device__ __forceinline__ bool in_bounds(bool ok, int* err) {
+  if (!ok && err) atomicOr(err, kErrBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool in_bounds(bool, int*) { return true; }
+#endif
 
 // ----------------------------------------------------------------- keys
 //

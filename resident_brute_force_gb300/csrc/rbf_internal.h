@@ -54,6 +54,7 @@ struct ScoreSelectLaunch {
   float* out_score = nullptr;
   int* err_sticky = nullptr;
   int* result_err = nullptr;
+  size_t partials_cap = 0;  // keys in partials, for checked builds (0: not checked)
 };
 
 // Shared memory the fused kernel needs for a launch shape.
@@ -76,6 +77,7 @@ struct MergeLaunch {
   uint64_t* kth_out = nullptr;  // optional: each query's K-th key
   int stride = 0;               // keys from one list to the next (0: list_width(k))
   const int* lens = nullptr;    // optional [queries x lists] valid keys per list (else all stride)
+  size_t partials_cap = 0;      // keys in partials, for checked builds (0: not checked)
   int short_lists = 0;          // 1: lists hold few valid keys (K > 32): stage a 32-key prefix of each
 };
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
@@ -87,6 +89,8 @@ struct I32Launch {
   uint64_t* partials;        // grid lists of list_width(k) keys
   int grid;
   const uint64_t* theta0 = nullptr;  // optional lower bound on the K-th key (keys >= it are kept)
+  size_t partials_cap = 0;           // keys in partials, for checked builds (0: not checked)
+  int* err = nullptr;                // error word for checked builds (may be null)
 };
 cudaError_t launch_topk_i32_stage1(const I32Launch& a, cudaStream_t stream);
 
@@ -109,6 +113,7 @@ struct I32StreamLaunch {
   int64_t* out_pos = nullptr;
   int* err_sticky = nullptr;
   int* result_err = nullptr;
+  size_t partials_cap = 0;     // keys in partials, for checked builds (0: not checked)
 };
 cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream);
 
@@ -149,6 +154,9 @@ struct GemmSelectLaunch {
   int* lens = nullptr;       // K > 32: [queries][grid] valid keys of each list (required)
   int wait_inputs = 1;       // 1: the kernel launched just before wrote the queries (the producer waits
                              // for it); 0: the corpus stream may start while that kernel finishes
+  size_t partials_cap = 0;   // keys in partials, lens entries, theta0 entries: for checked builds
+  size_t lens_cap = 0;       // (0: not checked)
+  size_t theta_cap = 0;
 };
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
 bool make_bf16_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);

@@ -62,6 +62,7 @@ struct Params {
   float* out_score;
   int* err_sticky;
   int* result_err;
+  size_t partials_cap;  // keys (checked builds; 0: not checked)
 };
 
 // NCH > 0: rows are exactly NCH * 128 floats and the query lives in
@@ -299,7 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
     }
     __syncthreads();
   }
-  if (warp == 0) warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
+  if (warp == 0 &&
+      in_bounds(p.partials_cap == 0 || (static_cast<size_t>(blockIdx.x) + 1) * KP <= p.partials_cap, p.err))
+    warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
 
   if (!p.dynamic && !p.out_idx) return;
   // The last CTA to finish re-arms the tile counter for the next launch and,
@@ -327,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
     o.q = 0;
     o.stride = KP;
     o.lens = nullptr;
+    o.region = static_cast<size_t>(gridDim.x) * KP;
+    o.err = p.err;
     // The ring only (the barriers after it are left alone).
     mergecore::merge_lists<KP, kThreads>(o, p.partials, static_cast<int>(gridDim.x), reinterpret_cast<uint64_t*>(smem),
                                          p.region_bytes, merge_stage_keys(p.region_bytes));
@@ -416,6 +421,7 @@ cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream)
   p.out_score = a.out_score;
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
+  p.partials_cap = a.partials_cap;
   const int smem = score_select_smem_bytes(a.pitch, a.k, a.rows_per_stage, a.stages);
   switch (list_width(a.k)) {
     case 32: return launch_kp<32>(p, a.grid, smem, a.normalize_query != 0, stream);

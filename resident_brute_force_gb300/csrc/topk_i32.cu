@@ -101,7 +101,8 @@ __device__ __forceinline__ void scan16(uint64_t (&v)[R], WarpBuffer& buf, int& c
 template <int KP>
 __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t* __restrict__ data, int64_t n,
                                                                   int k, uint64_t* partials,
-                                                                  const uint64_t* __restrict__ theta0) {
+                                                                  const uint64_t* __restrict__ theta0,
+                                                                  size_t partials_cap, int* err) {
   constexpr int R = KP / 32;
   __shared__ WarpBuffer bufs[NW];
   __shared__ __align__(16) uint64_t lists[NW * KP];
@@ -179,7 +180,8 @@ __global__ void __launch_bounds__(NW * 32) topk_i32_stage1_kernel(const int32_t*
     }
     __syncthreads();
   }
-  if (warp == 0) warp_list_store<R>(v, partials + static_cast<size_t>(blockIdx.x) * KP, lane);
+  if (warp == 0 && in_bounds(partials_cap == 0 || (static_cast<size_t>(blockIdx.x) + 1) * KP <= partials_cap, err))
+    warp_list_store<R>(v, partials + static_cast<size_t>(blockIdx.x) * KP, lane);
 }
 
 // Streaming variant for large arrays: the same per-warp selection, with the
@@ -221,6 +223,7 @@ struct StreamParams {
   int64_t* out_pos;
   int* err_sticky;
   int* result_err;
+  size_t partials_cap;  // keys (checked builds; 0: not checked)
 };
 
 // The last CTA merges in the ring's shared memory (the barriers after it are
@@ -432,7 +435,9 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     }
     __syncthreads();
   }
-  if (warp == 0) warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
+  if (warp == 0 &&
+      in_bounds(p.partials_cap == 0 || (static_cast<size_t>(blockIdx.x) + 1) * KP <= p.partials_cap, p.err))
+    warp_list_store<R>(v, p.partials + static_cast<size_t>(blockIdx.x) * KP, lane);
   __shared__ int s_last;
   __threadfence();  // this CTA's list is visible before its ticket
   __syncthreads();
@@ -457,6 +462,8 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     o.q = 0;
     o.stride = KP;
     o.lens = nullptr;
+    o.region = static_cast<size_t>(gridDim.x) * KP;
+    o.err = p.err;
     mergecore::merge_lists<KP, kSThreads>(o, p.partials, static_cast<int>(gridDim.x),
                                           reinterpret_cast<uint64_t*>(smem), kMergeSmemBytes, kMergeStageKeys);
     if (threadIdx.x == 0) {
@@ -495,7 +502,8 @@ __global__ void wait_probe_kernel(int* err, uint64_t timeout_ns) {
 
 template <int KP>
 cudaError_t launch_t(const I32Launch& a, cudaStream_t stream) {
-  topk_i32_stage1_kernel<KP><<<a.grid, NW * 32, 0, stream>>>(a.data, a.n, a.k, a.partials, a.theta0);
+  topk_i32_stage1_kernel<KP><<<a.grid, NW * 32, 0, stream>>>(a.data, a.n, a.k, a.partials, a.theta0, a.partials_cap,
+                                                              a.err);
   return cudaGetLastError();
 }
 
@@ -525,6 +533,7 @@ cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream
   p.out_pos = a.out_pos;
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
+  p.partials_cap = a.partials_cap;
   if (a.k < 1 || a.k > kBoundGroups) return cudaErrorInvalidValue;
   switch (list_width(a.k)) {
     case 32: return launch_stream_t<32>(p, a.grid, stream);
