@@ -564,6 +564,11 @@ def main():
             "k100_over_k8": round(per_k["100"]["p50_us"] / per_k["8"]["p50_us"], 3) if "100" in per_k else None,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks,
+            # The pages' number for this workload (1M x 1024, K = 8) is end to end on a
+            # GTX 1080: 114.12 ms per query = 35.9 GB/s. Context, not the target; vs_baseline
+            # stays null because that figure is end to end and `value` is device time.
+            "pages_context": {"e2e_gbs": 35.9, "hardware": "GTX 1080 (sm_61), end to end, mean of 3",
+                              "e2e_over_pages": round(e2e["value"] / 35.9, 1) if e2e else None},
         }
         if cosine is not None:
             line["cosine"] = cosine
