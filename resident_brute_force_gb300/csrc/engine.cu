@@ -225,7 +225,7 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_
   // Cosine mode: rows are unit length already; the kernel scales its copy of
   // the query to unit length, so the inner product is the cosine.
   a.normalize_query = (e->flags & RBF_FLAG_COSINE) ? 1 : 0;
-  const bool fuse = d_idx && score_select_can_merge(e->pitch, k, sh.rows_per_stage, sh.stages, sh.grid);
+  const bool fuse = d_idx && score_select_can_merge(e->pitch, k, sh.rows_per_stage, sh.stages);
   if (fuse) {
     a.out_idx = d_idx;
     a.out_score = d_score;
@@ -741,40 +741,54 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     RBF_LAUNCH(e, launch_to_bf16(d_queries, e->d, e->query_bf16, e->pitch_bf16, b, rows_total, e->d, e->num_sms,
                                  e->stream));
   }
-  // The scoring + select kernel over rows [0, rows): one launch per group of
-  // up to 256 queries; returns the number of per-CTA lists per query.
-  auto score_groups = [&](int64_t rows, int bound_mode, const uint64_t* theta0, int* lists) -> rbf_status {
-    // Clusters of two CTAs over 256-row tiles: an even grid, one list per
-    // query from each CTA of a pair (the CTA holds the query's TMEM lane)
-    // and column half, so grid lists per query.
+  // Clusters of two CTAs over 256-row tiles: an even grid, one list per
+  // query from each CTA of a pair (the CTA holds the query's TMEM lane) and
+  // column half, so grid lists per query.
+  auto grid_for = [&](int64_t rows) {
     const int64_t pair_tiles = (rows + 255) / 256;
-    const int grid = 2 * static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pair_tiles, e->num_sms / 2)));
+    return 2 * static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pair_tiles, e->num_sms / 2)));
+  };
+  // One launch of the scoring + select kernel over rows [0, rows) for the
+  // queries [q0, q0 + qc) (lists at q_out0 in the partials layout).
+  auto launch_group = [&](int64_t rows, int grid, int q0, int qc, int q_out0, int bound_mode, const uint64_t* theta0,
+                          bool wait_inputs) -> rbf_status {
+    GemmSelectLaunch a;
+    a.tmap_q = &e->tmap_query;
+    a.tmap_c = &e->tmap_corpus;
+    a.partials = e->partials;
+    a.err = e->errw;
+    a.n = rows;
+    a.kchunks = tf32 ? (e->d + 31) / 32 : e->pitch_bf16 / 64;
+    a.tf32 = tf32 ? 1 : 0;
+    a.q_row0 = q0;
+    a.q_count = qc;
+    a.q_out0 = q_out0;
+    a.k = k;
+    a.grid = grid;
+    a.timeout_ns = e->timeout_ns;
+    a.theta0 = theta0;
+    a.bound_mode = bound_mode;
+    a.lens = k > kBatchRegMaxK ? e->lens : nullptr;
+    a.partials_cap = device_cap(e);
+    a.lens_cap = static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms;
+    a.theta_cap = static_cast<size_t>(e->max_batch);
+    // Only the first launch after the query staging waits for it before
+    // streaming (after the bound merge, or another group, the queries are
+    // long complete).
+    a.wait_inputs = wait_inputs ? 1 : 0;
+    RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+    return RBF_OK;
+  };
+  // All groups of up to 256 queries over rows [0, rows), lists of 32 keys;
+  // returns the number of per-CTA lists per query.
+  auto score_groups = [&](int64_t rows, int bound_mode, const uint64_t* theta0, int* lists) -> rbf_status {
+    const int grid = grid_for(rows);
     if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;
     for (int q0 = 0; q0 < b; q0 += kBatchQueriesPerLaunch) {
-      GemmSelectLaunch a;
-      a.tmap_q = &e->tmap_query;
-      a.tmap_c = &e->tmap_corpus;
-      a.partials = e->partials;
-      a.err = e->errw;
-      a.n = rows;
-      a.kchunks = tf32 ? (e->d + 31) / 32 : e->pitch_bf16 / 64;
-      a.tf32 = tf32 ? 1 : 0;
-      a.q_row0 = q0;
-      a.q_count = std::min(kBatchQueriesPerLaunch, b - q0);
-      a.q_out0 = q0;
-      a.k = k;
-      a.grid = grid;
-      a.timeout_ns = e->timeout_ns;
-      a.theta0 = theta0;
-      a.bound_mode = bound_mode;
-      a.partials_cap = device_cap(e);
-      a.lens_cap = static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms;
-      a.theta_cap = static_cast<size_t>(e->max_batch);
-      // Only the first launch after the query staging waits for it before
-      // streaming (after the bound merge, or another group, the queries are
-      // long complete).
-      a.wait_inputs = (q0 == 0 && (bound_mode || theta0 == nullptr)) ? 1 : 0;
-      RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+      const int qc = std::min(kBatchQueriesPerLaunch, b - q0);
+      if (rbf_status st = launch_group(rows, grid, q0, qc, q0, bound_mode, theta0,
+                                       q0 == 0 && (bound_mode || theta0 == nullptr)))
+        return st;
     }
     *lists = grid;
     return RBF_OK;
@@ -822,34 +836,13 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   // list in the partials buffer with its length in `lens`) and merged before
   // the next group reuses the buffer. The last merge hands the call's error
   // word over.
-  const int64_t pair_tiles = (e->n + 255) / 256;
-  const int grid = 2 * static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pair_tiles, e->num_sms / 2)));
+  const int grid = grid_for(e->n);
   const int kw = list_width(k);
   if (static_cast<size_t>(kBatchQueriesPerLaunch) * grid * kw > e->partials_cap) return RBF_ERR_UNSUPPORTED;
   for (int q0 = 0; q0 < b; q0 += kBatchQueriesPerLaunch) {
     const int qc = std::min(kBatchQueriesPerLaunch, b - q0);
     const bool last = q0 + qc == b;
-    GemmSelectLaunch a;
-    a.tmap_q = &e->tmap_query;
-    a.tmap_c = &e->tmap_corpus;
-    a.partials = e->partials;
-    a.err = e->errw;
-    a.n = e->n;
-    a.kchunks = tf32 ? (e->d + 31) / 32 : e->pitch_bf16 / 64;
-    a.tf32 = tf32 ? 1 : 0;
-    a.q_row0 = q0;
-    a.q_count = qc;
-    a.q_out0 = 0;
-    a.k = k;
-    a.grid = grid;
-    a.timeout_ns = e->timeout_ns;
-    a.theta0 = theta0;
-    a.lens = e->lens;
-    a.partials_cap = device_cap(e);
-    a.lens_cap = static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms;
-    a.theta_cap = static_cast<size_t>(e->max_batch);
-    a.wait_inputs = (q0 == 0 && theta0 == nullptr) ? 1 : 0;
-    RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
+    if (rbf_status st = launch_group(e->n, grid, q0, qc, 0, 0, theta0, q0 == 0 && theta0 == nullptr)) return st;
     MergeLaunch m;
     m.partials = e->partials;
     m.lists = grid;

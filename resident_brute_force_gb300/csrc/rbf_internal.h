@@ -60,7 +60,7 @@ struct ScoreSelectLaunch {
 // Shared memory the fused kernel needs for a launch shape.
 int score_select_smem_bytes(int pitch, int k, int rows_per_stage, int stages);
 // Whether the kernel's ring can hold its last CTA's merge for this shape.
-bool score_select_can_merge(int pitch, int k, int rows_per_stage, int stages, int grid);
+bool score_select_can_merge(int pitch, int k, int rows_per_stage, int stages);
 cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream);
 
 struct MergeLaunch {

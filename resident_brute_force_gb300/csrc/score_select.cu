@@ -387,11 +387,10 @@ int region_bytes(int pitch, int k, int rows_per_stage, int stages) {
 
 }  // namespace
 
-bool score_select_can_merge(int pitch, int k, int rows_per_stage, int stages, int grid) {
+bool score_select_can_merge(int pitch, int k, int rows_per_stage, int stages) {
   // The general merge needs a tree of one list per warp plus one staged
   // list; the fast path applies when its staging fits as well.
   const int keys = region_bytes(pitch, k, rows_per_stage, stages) / 8;
-  (void)grid;
   return keys >= (kThreads / 32) * list_width(k) + k;
 }
 
