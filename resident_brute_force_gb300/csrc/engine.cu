@@ -67,8 +67,8 @@ struct rbf_engine {
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
-  alignas(64) CUtensorMap tmap_corpus;
-  alignas(64) CUtensorMap tmap_query;
+  CUtensorMap tmap_corpus;  // the type carries the alignment a tensor map needs
+  CUtensorMap tmap_query;
   bool tmaps_ready = false;
 
   // Workspaces (device).

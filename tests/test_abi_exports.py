@@ -58,3 +58,14 @@ def test_product_path_does_not_touch_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 for bad in ("import oracle", "from oracle", "liboracle", "oracle.c"):
                     assert bad not in text, (f, bad)
+
+
+def test_checked_build_exports_the_same_boundary():
+    """The checked build (-DRBF_CHECKS) compiles, exports every declared
+    function and names its extra status."""
+    from resident_brute_force_gb300 import _build
+    checked = ctypes.CDLL(_build.build(checks=True))
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    checked.rbf_status_string.restype = ctypes.c_char_p
+    assert checked.rbf_status_string(7) == b"RBF_ERR_BOUNDS"
