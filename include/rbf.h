@@ -113,8 +113,10 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
  * that as a limitation; CUDA programming model series 9, section 4.2, runs
  * independent top-K work on separate streams). The view takes the base's
  * sizes, flags and options; set_option on a view changes only the view.
- * An upload on the base is seen by its views at their next call; it must not
- * overlap a call on any view. Views cannot upload.
+ * An upload on the base first waits for the work already queued on its views'
+ * streams, and its views see the new corpus at their next call; the upload
+ * call itself must not run at the same time as a call on a view (from another
+ * host thread). Views cannot upload.
  *   base         an engine made by rbf_create (not a view)
  *   cuda_stream  a cudaStream_t, or NULL for a view-owned non-blocking stream
  *   out          receives the view handle (destroy it with rbf_destroy,

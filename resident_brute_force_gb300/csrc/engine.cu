@@ -16,6 +16,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "../../include/rbf.h"
 #include "rbf_device.cuh"
@@ -107,11 +108,11 @@ struct rbf_engine {
   int fault_count = 0;
 
   // Views (rbf_create_view): a view searches its owner's corpus with its own
-  // stream and per-call buffers. The owner counts its views and bumps
-  // corpus_version around every upload; a view re-reads the corpus state
-  // when the version it saw is stale.
+  // stream and per-call buffers. The owner lists its views (an upload waits
+  // for their streams) and bumps corpus_version around every upload; a view
+  // re-reads the corpus state when the version it saw is stale.
   rbf_engine* owner = nullptr;
-  int views = 0;
+  std::vector<rbf_engine*> views;
   unsigned corpus_version = 0;
   unsigned seen_version = 0;
 };
@@ -296,7 +297,8 @@ void release(rbf_engine* e) {
   if (e->stream) cudaStreamSynchronize(e->stream);
   drop_graphs(e);
   if (e->owner) {
-    --e->owner->views;  // the corpus belongs to the owner
+    auto& v = e->owner->views;  // the corpus belongs to the owner
+    v.erase(std::remove(v.begin(), v.end(), e), v.end());
   } else {
     cudaFree(e->corpus);
     cudaFree(e->corpus_bf16);
@@ -508,7 +510,13 @@ rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out
   e->batch_sample = base->batch_sample;
   e->owner = base;
   e->seen_version = base->corpus_version - 1;  // read the corpus state at the first call
-  ++base->views;
+  try {
+    base->views.push_back(e);
+  } catch (...) {
+    e->owner = nullptr;
+    release(e);
+    return RBF_ERR_OUT_OF_MEMORY;
+  }
   if (cuda_stream) {
     e->stream = static_cast<cudaStream_t>(cuda_stream);
   } else if (cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking) != cudaSuccess) {
@@ -524,7 +532,7 @@ rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out
 }
 
 rbf_status rbf_destroy(rbf_engine* e) {
-  if (e && e->views > 0) return RBF_ERR_INVALID_VALUE;
+  if (e && !e->views.empty()) return RBF_ERR_INVALID_VALUE;
   release(e);
   return RBF_OK;
 }
@@ -592,6 +600,7 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
   e->ready = false;
   ++e->corpus_version;  // views re-read the corpus state at their next call
   cudaStreamSynchronize(e->stream);
+  for (rbf_engine* v : e->views) cudaStreamSynchronize(v->stream);  // their searches in flight read the corpus
   drop_graphs(e);  // captured launches carry the old corpus shape
   const int pitch = static_cast<int>(align_up(static_cast<size_t>(d), 4));
   RBF_COPY(e, cudaMemcpy2DAsync(e->corpus, static_cast<size_t>(pitch) * 4, corpus, static_cast<size_t>(d) * 4,

@@ -208,3 +208,36 @@ def test_concurrent_batched_and_int32_on_views(rbf):
         for h in hs[1:]:
             h.close()
         base.close()
+
+
+def test_upload_waits_for_searches_queued_on_views(rbf):
+    """A view queues device searches over a 400 MB corpus (a few ms of work in
+    flight) and the base uploads a different corpus right away: every queued
+    search must still see the old corpus, and the next one the new."""
+    import torch
+    n, d, k, nq = 100_000, 1024, 8, 24
+    c1 = workloads.unit_corpus(n, d, seed=94)
+    c2 = -c1                                            # same shape, every score negated
+    qs = workloads.unit_queries(nq, d, seed=95)
+    st = torch.cuda.Stream()
+    base = rbf.Engine(n, d, k)
+    base.upload_corpus_rowmajor(c1)
+    v = base.view(stream=st)
+    try:
+        dq = torch.from_numpy(qs).cuda()
+        dc2 = torch.from_numpy(c2).cuda()
+        out_i = torch.zeros((nq, k), dtype=torch.int32, device="cuda")
+        out_s = torch.zeros((nq, k), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            for j in range(nq):
+                v.search_resident_dev(dq[j], k, out_i[j], out_s[j])
+        base.upload_corpus_rowmajor(dc2)                # no synchronisation with the view's stream
+        torch.cuda.synchronize()
+        for j in range(0, nq, 5):
+            check_float_topk(out_i[j].cpu().numpy(), out_s[j].cpu().numpy(), oracle.scores(c1, qs[j]), k)
+        check_float_topk(*v.search_resident(qs[0], k), oracle.scores(c2, qs[0]), k)
+        assert v.check_device_error() == rbf.RBF_OK
+    finally:
+        v.close()
+        base.close()
