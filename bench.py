@@ -182,6 +182,26 @@ def result_d2h_bytes(k: int) -> int:
     return b_off + 4 * k
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def cpu_oracle_rate(c, qs, k, budget_s=12.0, max_queries=200, row_sample=None):
     """Time the oracle as it stands on this host. Returns (GB/s, cores, sample text, per-query seconds)."""
     import oracle
@@ -549,7 +569,17 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, cores, sample, _ = cpu_oracle_rate(c, qs, 8)
-        cpu = {"value": round(rate, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = {"value": round(rate, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "cpu_model": cpu_model()}
+        # The same oracle on one core (scoring no longer split over threads).
+        import oracle
+        o = oracle.get()
+        o.set_num_threads(1)
+        try:
+            rate1, _, sample1, _ = cpu_oracle_rate(c, qs, 8, budget_s=4.0, max_queries=3)
+        finally:
+            o.set_num_threads(cores)
+        cpu["one_core"] = {"value": round(rate1, 3), "sample": sample1}
 
     if rank == 0:
         line = {
