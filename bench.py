@@ -78,6 +78,20 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def device_info(gpu=0):
+    """GPU name, driver version and CUDA runtime of the run (nvidia-smi for the driver)."""
+    import subprocess
+    import torch
+    info = {"name": torch.cuda.get_device_name(gpu), "cuda_runtime": torch.version.cuda, "driver": None}
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(gpu), "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        info["driver"] = out or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return info
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -593,7 +607,7 @@ def main():
             "p50_us": per_k["8"]["p50_us"], "p99_us": per_k["8"]["p99_us"], "per_k": per_k,
             "k100_over_k8": round(per_k["100"]["p50_us"] / per_k["8"]["p50_us"], 3) if "100" in per_k else None,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks,
+            "gpu_launches": args.steps, "clocks": clocks, "device": device_info(local),
             # The pages' number for this workload (1M x 1024, K = 8) is end to end on a
             # GTX 1080: 114.12 ms per query = 35.9 GB/s. Context, not the target; vs_baseline
             # stays null because that figure is end to end and `value` is device time.
