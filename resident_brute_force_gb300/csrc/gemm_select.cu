@@ -241,8 +241,12 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
   return a;
 }
+// Arrival on a barrier of either CTA of the cluster that orders no memory:
+// it only says that the arriving warp's TMEM loads have completed
+// (tcgen05.wait::ld returned and tcgen05.fence::before_thread_sync issued),
+// and a release at cluster scope would cost a fence per arrival.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
