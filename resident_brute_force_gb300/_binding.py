@@ -104,6 +104,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
 def topk_int32_noalloc(d_data, k: int, d_val, d_pos, stream=None) -> int:
     """Call topk_int32_noalloc (no engine, no device allocation); returns the
     status code. All tensors are CUDA tensors on the current device."""
+    _need(d_val.numel() >= max(int(k), 0) and d_pos.numel() >= max(int(k), 0),
+          f"d_val / d_pos hold {d_val.numel()} / {d_pos.numel()} entries, the call writes {k}")
     s = None
     if stream is not None:
         s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -141,6 +143,13 @@ def _dev_ptr(t, dtype_name: str) -> int:
     return t.data_ptr()
 
 
+def _need(ok: bool, msg: str) -> None:
+    """The library reads and writes exactly the sizes it is given; a buffer
+    that is too short is refused here, before any pointer reaches it."""
+    if not ok:
+        raise ValueError(msg)
+
+
 def _any_ptr(x, np_dtype, torch_dtype_name: str) -> tuple[object, int]:
     """Pointer to host (numpy / CPU tensor) or device (CUDA tensor) data."""
     if hasattr(x, "data_ptr"):
@@ -172,8 +181,24 @@ class Engine:
         self._h = handle
         self._stream_ref = stream
         self._base = _view_of  # a view keeps its base alive
-        self.d = _view_of.d if _view_of is not None else None
-        self.n = _view_of.n if _view_of is not None else None
+        self._n = None
+        self._d = None
+
+    @property
+    def n(self):
+        """Rows of the resident corpus (None before an upload); a view reports its base's."""
+        return self._base.n if self._base is not None else self._n
+
+    @property
+    def d(self):
+        """Dimension of the resident corpus (None before an upload); a view reports its base's."""
+        return self._base.d if self._base is not None else self._d
+
+    def _out_len(self, t, count: int, what: str) -> None:
+        _need(t.numel() >= max(int(count), 0), f"{what} holds {t.numel()} entries, the call writes {count}")
+
+    def _query_len(self, size: int, what: str) -> None:
+        _need(self.d is None or size == self.d, f"{what} has {size} elements, the corpus has D = {self.d}")
 
     def view(self, stream=None) -> "Engine":
         """A second handle on this engine's resident corpus with its own stream
@@ -236,15 +261,17 @@ class Engine:
 
     # -- ingest
     def upload_corpus_rowmajor(self, corpus) -> None:
+        _need(len(corpus.shape) == 2, "the corpus is a 2-D [N, D] array")
         keep, ptr = _any_ptr(corpus, np.float32, "float32")
         n, d = corpus.shape
         self._check(self.lib.upload_corpus_rowmajor(self._h, ptr, int(n), int(d)), "upload_corpus_rowmajor")
-        self.n, self.d = int(n), int(d)
+        self._n, self._d = int(n), int(d)
         del keep
 
     # -- single query
     def search_resident(self, query, k: int):
         q, qp = _host_ptr(np.asarray(query).reshape(-1), np.float32)
+        self._query_len(q.size, "the query")
         idx = np.empty(max(int(k), 0), dtype=np.int32)
         sc = np.empty(max(int(k), 0), dtype=np.float32)
         self._check(self.lib.search_resident(self._h, qp, int(k), idx.ctypes.data, sc.ctypes.data),
@@ -252,21 +279,29 @@ class Engine:
         return idx, sc
 
     def search_resident_dev(self, d_query, k: int, d_idx, d_score) -> None:
+        self._query_len(d_query.numel(), "d_query")
+        self._out_len(d_idx, k, "d_idx")
+        self._out_len(d_score, k, "d_score")
         self._check(self.lib.search_resident_dev(self._h, _dev_ptr(d_query, "float32"), int(k),
                                                  _dev_ptr(d_idx, "int32"), _dev_ptr(d_score, "float32")),
                     "search_resident_dev")
 
     def score_select_partials_dev(self, d_query, k: int) -> None:
+        self._query_len(d_query.numel(), "d_query")
         self._check(self.lib.score_select_partials_dev(self._h, _dev_ptr(d_query, "float32"), int(k)),
                     "score_select_partials_dev")
 
     def merge_partial_topk_dev(self, k: int, d_idx, d_score) -> None:
+        self._out_len(d_idx, k, "d_idx")
+        self._out_len(d_score, k, "d_score")
         self._check(self.lib.merge_partial_topk_dev(self._h, int(k), _dev_ptr(d_idx, "int32"),
                                                     _dev_ptr(d_score, "float32")), "merge_partial_topk_dev")
 
     # -- batched
     def search_resident_batch(self, queries, k: int):
         q, qp = _host_ptr(np.asarray(queries), np.float32)
+        _need(q.ndim == 2, "the queries are a 2-D [B, D] array")
+        self._query_len(q.shape[1], "each query")
         b = q.shape[0]
         idx = np.empty((b, max(int(k), 0)), dtype=np.int32)
         sc = np.empty((b, max(int(k), 0)), dtype=np.float32)
@@ -275,7 +310,11 @@ class Engine:
         return idx, sc
 
     def search_resident_batch_dev(self, d_queries, k: int, d_idx, d_score) -> None:
+        _need(d_queries.dim() == 2, "d_queries is a 2-D [B, D] tensor")
+        self._query_len(d_queries.shape[1], "each query of d_queries")
         b = d_queries.shape[0]
+        self._out_len(d_idx, b * int(k), "d_idx")
+        self._out_len(d_score, b * int(k), "d_score")
         self._check(self.lib.search_resident_batch_dev(self._h, _dev_ptr(d_queries, "float32"), int(b), int(k),
                                                        _dev_ptr(d_idx, "int32"), _dev_ptr(d_score, "float32")),
                     "search_resident_batch_dev")
@@ -289,5 +328,7 @@ class Engine:
         return val, pos
 
     def topk_int32_dev(self, d_data, k: int, d_val, d_pos) -> None:
+        self._out_len(d_val, k, "d_val")
+        self._out_len(d_pos, k, "d_pos")
         self._check(self.lib.topk_int32_dev(self._h, _dev_ptr(d_data, "int32"), int(d_data.numel()), int(k),
                                             _dev_ptr(d_val, "int32"), _dev_ptr(d_pos, "int64")), "topk_int32_dev")

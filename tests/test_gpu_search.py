@@ -209,6 +209,41 @@ def test_argument_errors(rbf):
         rbf.Engine(10, 16, max_k=257)
 
 
+def test_binding_refuses_short_buffers(rbf):
+    """The C entry points read and write exactly the sizes they are given; the
+    binding refuses a query of the wrong length or an output that is too short
+    before any pointer reaches the library, and the engine stays usable."""
+    import torch
+    n, d, k = 2000, 64, 16
+    c = workloads.dyadic_grid(n, d, seed=52)
+    with make_engine(rbf, n, d, max_k=64, max_batch=4) as e:
+        e.upload_corpus_rowmajor(c)
+        assert (e.n, e.d) == (n, d)
+        dq = torch.from_numpy(c[3]).cuda()
+        di = torch.empty(k, dtype=torch.int32, device="cuda")
+        ds = torch.empty(k, dtype=torch.float32, device="cuda")
+        bad = [
+            lambda: e.search_resident(c[3][:d - 1], k),
+            lambda: e.search_resident_dev(dq[:d - 1], k, di, ds),
+            lambda: e.search_resident_dev(dq, k, di[:k - 1], ds),
+            lambda: e.search_resident_dev(dq, k, di, ds[:k - 1]),
+            lambda: e.score_select_partials_dev(dq[:d - 1], k),
+            lambda: e.merge_partial_topk_dev(k, di[:k - 1], ds),
+            lambda: e.search_resident_batch(c[:2, :d - 1], k),
+            lambda: e.search_resident_batch(c[3], k),
+            lambda: e.search_resident_batch_dev(torch.from_numpy(c[:2]).cuda(), k, di, ds),
+            lambda: e.topk_int32_dev(di, k, di[:k - 1], torch.empty(k, dtype=torch.int64, device="cuda")),
+            lambda: rbf.topk_int32_noalloc(di, k, di, torch.empty(k - 1, dtype=torch.int64, device="cuda")),
+            lambda: e.upload_corpus_rowmajor(c[0]),
+        ]
+        for j, call in enumerate(bad):
+            with pytest.raises(ValueError):
+                call()
+        torch.cuda.synchronize()
+        check_exact(*e.search_resident(c[3], k), *oracle.topk(c, c[3], k))
+        assert e.check_device_error() == rbf.RBF_OK
+
+
 def test_bounded_wait_timeout_reports_and_context_survives(rbf):
     c = workloads.dyadic_grid(1000, 64, seed=61)
     with make_engine(rbf, 1000, 64) as e:

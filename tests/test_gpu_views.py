@@ -136,6 +136,7 @@ def test_upload_on_base_reaches_views_and_rules(rbf):
         base.upload_corpus_rowmajor(c1)
         check_exact(*v.search_resident(q1, k), *oracle.topk(c1, q1, k))  # captures a graph
         base.upload_corpus_rowmajor(c2)                 # new shape: the view's graph must go
+        assert (v.n, v.d) == (n // 2, d + 3)
         check_exact(*v.search_resident(q2, k), *oracle.topk(c2, q2, k))
         with pytest.raises(rbf.RbfError) as ei:
             v.upload_corpus_rowmajor(c1)                # views cannot upload
