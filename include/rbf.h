@@ -167,9 +167,13 @@ rbf_status upload_corpus_rowmajor(rbf_engine* engine, const float* corpus, int64
 /* ---------------------------------------------------------- single query */
 
 /* Top-K of one query against the resident corpus (the article's
- * search_resident, section 4 steps 2-6): H2D of the D-float query, the fused
- * score + per-CTA partial top-K kernel, the merge kernel, D2H of K indices and
- * K scores.
+ * search_resident, section 4 steps 2-6: query to the device, scoring,
+ * per-block partial top-K, merge, results back). Here the query is copied
+ * into the engine's pinned staging block, which the scoring kernel reads in
+ * place; one launch scores every row, keeps per-CTA top-K lists and merges
+ * them in its last CTA, writing the K results straight into the pinned
+ * result block; the call returns after synchronising the engine's stream.
+ * The launch is a CUDA graph captured on the first call for each k.
  *   query      host, D floats (D of the resident corpus)
  *   k          1 .. min(max_k, N)
  *   out_idx    host, K int32 row indices, best-first
