@@ -48,7 +48,7 @@ typedef enum rbf_status {
   RBF_ERR_OUT_OF_MEMORY = 3, /* rbf_create could not allocate */
   RBF_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   RBF_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
-  RBF_ERR_UNSUPPORTED = 6,   /* valid request this build does not handle */
+  RBF_ERR_UNSUPPORTED = 6,   /* valid request beyond the engine's launch limits */
   RBF_ERR_BOUNDS = 7         /* checked builds (RBF_CHECKS) only: a kernel met an index outside
                                 its buffer and skipped the access; the outputs are not valid */
 } rbf_status;
