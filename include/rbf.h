@@ -116,7 +116,8 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
  * An upload on the base first waits for the work already queued on its views'
  * streams, and its views see the new corpus at their next call; the upload
  * call itself must not run at the same time as a call on a view (from another
- * host thread). Views cannot upload.
+ * host thread). Views cannot upload. Views may be made and destroyed from
+ * any host thread, also while other views of the same base are in use.
  *   base         an engine made by rbf_create (not a view)
  *   cuda_stream  a cudaStream_t, or NULL for a view-owned non-blocking stream
  *   out          receives the view handle (destroy it with rbf_destroy,

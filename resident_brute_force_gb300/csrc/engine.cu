@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -113,6 +114,7 @@ struct rbf_engine {
   // re-reads the corpus state when the version it saw is stale.
   rbf_engine* owner = nullptr;
   std::vector<rbf_engine*> views;
+  std::mutex views_mu;  // views may be made and destroyed from several host threads
   unsigned corpus_version = 0;
   unsigned seen_version = 0;
 };
@@ -297,7 +299,8 @@ void release(rbf_engine* e) {
   if (e->stream) cudaStreamSynchronize(e->stream);
   drop_graphs(e);
   if (e->owner) {
-    auto& v = e->owner->views;  // the corpus belongs to the owner
+    std::lock_guard<std::mutex> lock(e->owner->views_mu);  // the corpus belongs to the owner
+    auto& v = e->owner->views;
     v.erase(std::remove(v.begin(), v.end(), e), v.end());
   } else {
     cudaFree(e->corpus);
@@ -511,6 +514,7 @@ rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out
   e->owner = base;
   e->seen_version = base->corpus_version - 1;  // read the corpus state at the first call
   try {
+    std::lock_guard<std::mutex> lock(base->views_mu);
     base->views.push_back(e);
   } catch (...) {
     e->owner = nullptr;
@@ -532,7 +536,10 @@ rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out
 }
 
 rbf_status rbf_destroy(rbf_engine* e) {
-  if (e && !e->views.empty()) return RBF_ERR_INVALID_VALUE;
+  if (e) {
+    std::lock_guard<std::mutex> lock(e->views_mu);
+    if (!e->views.empty()) return RBF_ERR_INVALID_VALUE;
+  }
   release(e);
   return RBF_OK;
 }
@@ -600,7 +607,10 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
   e->ready = false;
   ++e->corpus_version;  // views re-read the corpus state at their next call
   cudaStreamSynchronize(e->stream);
-  for (rbf_engine* v : e->views) cudaStreamSynchronize(v->stream);  // their searches in flight read the corpus
+  {
+    std::lock_guard<std::mutex> lock(e->views_mu);
+    for (rbf_engine* v : e->views) cudaStreamSynchronize(v->stream);  // their searches in flight read the corpus
+  }
   drop_graphs(e);  // captured launches carry the old corpus shape
   const int pitch = static_cast<int>(align_up(static_cast<size_t>(d), 4));
   RBF_COPY(e, cudaMemcpy2DAsync(e->corpus, static_cast<size_t>(pitch) * 4, corpus, static_cast<size_t>(d) * 4,

@@ -242,3 +242,38 @@ def test_upload_waits_for_searches_queued_on_views(rbf):
     finally:
         v.close()
         base.close()
+
+
+def test_views_made_and_destroyed_from_threads(rbf):
+    """Four host threads each make a view, search with it and destroy it, five
+    times over, while the others do the same: every result equals the base's
+    and the base can be closed afterwards (no view left behind)."""
+    n, d, k = 20_000, 128, 16
+    c = workloads.dyadic_grid(n, d, seed=96)
+    qs = workloads.dyadic_grid(40, d, seed=97)
+    base = rbf.Engine(n, d, k)
+    base.upload_corpus_rowmajor(c)
+    expect = [base.search_resident(qs[j], k) for j in range(40)]
+    errors = []
+
+    def worker(t):
+        try:
+            for rep in range(5):
+                with base.view() as v:
+                    for j in range(t, 40, 4):
+                        idx, sc = v.search_resident(qs[j], k)
+                        if not (np.array_equal(idx, expect[j][0]) and np.array_equal(sc, expect[j][1])):
+                            errors.append((t, rep, j))
+        except Exception as ex:  # pragma: no cover - reported below
+            errors.append((t, repr(ex)))
+
+    try:
+        threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        assert not errors, errors[:5]
+        check_exact(*expect[7], *oracle.topk(c, qs[7], k))
+    finally:
+        base.close()
