@@ -194,7 +194,13 @@ def test_argument_errors(rbf):
         assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
         with pytest.raises(rbf.RbfError):
             e.upload_corpus_rowmajor(np.zeros((10, 17), np.float32))
+        with pytest.raises(rbf.RbfError) as ei:
+            e.upload_corpus_rowmajor(np.zeros((0, 16), np.float32))   # empty corpus
+        assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
         e.upload_corpus_rowmajor(c[:50])
+        with pytest.raises(rbf.RbfError) as ei:
+            e.search_resident_batch(np.zeros((0, 16), np.float32), 4)  # empty batch
+        assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
         for k in (0, -1, 65, 51):
             with pytest.raises(rbf.RbfError) as ei:
                 e.search_resident(q, k)

@@ -87,6 +87,9 @@ def test_argument_errors(eng):
         with pytest.raises(rbf.RbfError) as ei:
             eng.topk_int32(d, k)
         assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
+    with pytest.raises(rbf.RbfError) as ei:
+        eng.topk_int32(d[:0], 1)                                  # empty array
+    assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
 
 
 def test_full_size_1e8(eng):
