@@ -431,7 +431,9 @@ def run_int32(rbf, steps, warmup):
     x = torch.from_numpy(workloads.int32_uniform(n, seed=1)).cuda()
     st = torch.cuda.Stream()
     e = rbf.Engine(16, 16, 64, stream=st)
-    out = {"workload": "n=100,000,000 int32 uniform over the full range"}
+    out = {"workload": "n=100,000,000 int32 uniform over the full range",
+           # The two-stage page's own kernel times for n = 1e8 (context, other hardware).
+           "pages_context": {"k20_ms": 8.7, "k50_ms": 15.1, "hardware": "Tesla V100, GRID 64 x BLOCK 256"}}
     dv = torch.empty(64, dtype=torch.int32, device="cuda")
     dp = torch.empty(64, dtype=torch.int64, device="cuda")
     hbm, _ = hbm_peak()
