@@ -69,3 +69,22 @@ def test_reference_arm_two_ranks():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_single_rank_line():
+    """The reference arm at N = 1: one JSON line with the contract's keys, the
+    CPU-baseline record describing this run, and zero-byte e2e transfers."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "1"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 1 and rec["steps"] == 2 and rec["value"] > 0
+    cpu = rec["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == rec["value"] and cpu["cores"] >= 1 and cpu["sample"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
