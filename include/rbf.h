@@ -148,6 +148,10 @@ const char* rbf_status_string(rbf_status status);
 /* cudaError_t value of the most recent RBF_ERR_CUDA on this engine. */
 int32_t rbf_last_cuda_error(const rbf_engine* engine);
 
+/* Number of kernels the engine's most recent search or top-K call enqueued
+ * (a replayed graph counts the kernels captured in it); 0 before any call. */
+int32_t rbf_last_launches(const rbf_engine* engine);
+
 /* Synchronise the stream and return (and clear) any error a device kernel
  * recorded since the last check: RBF_ERR_TIMEOUT if a bounded wait ran out,
  * RBF_ERR_BOUNDS if a checked build skipped an access outside its buffer. */
@@ -253,11 +257,20 @@ rbf_status topk_int32_dev(rbf_engine* engine, const int32_t* d_data, int64_t n, 
  * code that cannot wait for an allocation. The retrieval pages have no
  * counterpart to this entry point.
  *
- * Needs no engine. It runs the same two kernels as topk_int32_dev with the
- * same result; their scratch (one 256-key list per stage-1 CTA, at most 512
- * lists) is a fixed 1 MiB array in the library's own device memory, which
- * every GPU that loads the library keeps until the process exits. Nothing is
- * allocated or freed, here or by any library routine it calls.
+ * Needs no engine. It gives the same result as topk_int32_dev, computed by
+ * the register-load stage-1 kernel (at most 512 CTAs, each keeping a top-K of
+ * a contiguous range) followed by the merge kernel. That is the pair
+ * topk_int32_dev uses below 262,144 elements; from that size on
+ * topk_int32_dev runs the one-launch bulk-copy stream kernel instead, which
+ * this entry point does not, so it is slower on large arrays. Neither of its
+ * two kernels waits on anything, so no call can time out. Their only scratch
+ * (one 256-key list per stage-1 CTA, at most 512 lists) is a fixed 1 MiB
+ * array in the library's own device memory, which every GPU that loads the
+ * library keeps until the process exits. The call allocates and frees
+ * nothing, and calls no allocating library routine; the array's memory is
+ * committed when the library's device code is loaded on a device, which with
+ * CUDA's lazy module loading (the default) can happen inside the first call
+ * on that device and may synchronise it, so make that first call at set-up.
  *   d_data    device, n int32 (4-byte aligned), on the current device
  *   n         1 .. 2^32-1
  *   k         1 .. min(RBF_MAX_K, n); a larger k is rejected with
@@ -271,7 +284,9 @@ rbf_status topk_int32_dev(rbf_engine* engine, const int32_t* d_data, int64_t n, 
  * stream capture. Every call shares the one array and it keeps the previous
  * call's contents; each call writes every list it reads, so nothing needs
  * clearing, but calls whose kernels overlap on the GPU (two streams, or two
- * host threads) race on the array: serialise them.
+ * host threads) race on the array: serialise them. The checked build
+ * (RBF_CHECKS) cannot report a skipped out-of-bounds access here, as there is
+ * no error word to report it through.
  * Errors: INVALID_VALUE (arguments), CUDA (lookup or launch failed). */
 rbf_status topk_int32_noalloc(const int32_t* d_data, int64_t n, int32_t k, int32_t* d_val, int64_t* d_pos,
                               void* cuda_stream);

@@ -56,6 +56,7 @@ SIGNATURES = {
     "rbf_set_option": (_S, [_P, _S, _I64]),
     "rbf_status_string": (ctypes.c_char_p, [_S]),
     "rbf_last_cuda_error": (_I32, [_P]),
+    "rbf_last_launches": (_I32, [_P]),
     "rbf_check_device_error": (_S, [_P]),
     "upload_corpus_rowmajor": (_S, [_P, _P, _I64, _I32]),
     "search_resident": (_S, [_P, _P, _I32, _P, _P]),
@@ -246,6 +247,11 @@ class Engine:
 
     def last_cuda_error(self) -> int:
         return self.lib.rbf_last_cuda_error(self._h)
+
+    @property
+    def last_launches(self) -> int:
+        """Kernels the most recent search / top-K call enqueued."""
+        return self.lib.rbf_last_launches(self._h)
 
     def set_option(self, option: int, value: int) -> None:
         self._check(self.lib.rbf_set_option(self._h, int(option), int(value)), "rbf_set_option")

@@ -92,6 +92,7 @@ struct rbf_engine {
   // captured on first use and dropped whenever the corpus or an option changes.
   cudaGraphExec_t host_graph[RBF_MAX_K + 1] = {};
   int host_graph_lists[RBF_MAX_K + 1] = {};
+  int host_graph_launches[RBF_MAX_K + 1] = {};
 
   // Options.
   int ctas_per_sm = 1;
@@ -105,6 +106,7 @@ struct rbf_engine {
   int last_k = 0;
 
   int last_cuda_error = 0;
+  int launches = 0;  // kernels enqueued by the most recent call (rbf_last_launches)
   int fault_kind = 0;
   int fault_count = 0;
 
@@ -161,6 +163,7 @@ size_t device_cap(const rbf_engine* e) {
     if (inject((e), 2)) return RBF_ERR_CUDA;           \
     cudaError_t _st = (call);                          \
     if (_st != cudaSuccess) return cuda_fail((e), _st); \
+    ++(e)->launches;                                   \
   } while (0)
 
 struct ScoreShape {
@@ -556,6 +559,8 @@ int32_t rbf_num_partials(const rbf_engine* e) {
 
 int32_t rbf_last_cuda_error(const rbf_engine* e) { return e ? e->last_cuda_error : 0; }
 
+int32_t rbf_last_launches(const rbf_engine* e) { return e ? e->launches : 0; }
+
 rbf_status rbf_set_option(rbf_engine* e, rbf_option opt, int64_t value) {
   if (!e) return RBF_ERR_INVALID_VALUE;
   cudaStreamSynchronize(e->stream);
@@ -658,6 +663,7 @@ rbf_status score_select_partials_dev(rbf_engine* e, const float* d_query, int32_
   if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
+  e->launches = 0;
   return enqueue_score(e, d_query, k);
 }
 
@@ -666,6 +672,7 @@ rbf_status merge_partial_topk_dev(rbf_engine* e, int32_t k, int32_t* d_idx, floa
   if (rbf_status s = sync_view(e)) return s;
   if (!e->ready || e->last_lists == 0) return RBF_ERR_NOT_READY;
   if (k != e->last_k) return RBF_ERR_INVALID_VALUE;
+  e->launches = 0;
   return enqueue_merge(e, k, e->last_lists, 1, 0, d_idx, d_score, reinterpret_cast<int*>(e->result));
 }
 
@@ -674,6 +681,7 @@ rbf_status search_resident_dev(rbf_engine* e, const float* d_query, int32_t k, i
   if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
+  e->launches = 0;
   bool merged = false;
   if (rbf_status s = enqueue_score(e, d_query, k, d_idx, d_score, reinterpret_cast<int*>(e->result), &merged))
     return s;
@@ -714,6 +722,7 @@ static rbf_status capture_host_search(rbf_engine* e, int k, const ResultLayout& 
   if (st != cudaSuccess) return cuda_fail(e, st);
   e->host_graph[k] = exec;
   e->host_graph_lists[k] = e->last_lists;
+  e->host_graph_launches[k] = e->launches;
   return RBF_OK;
 }
 
@@ -727,6 +736,7 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
   if (inject(e, 1)) return RBF_ERR_CUDA;
   std::memcpy(e->h_query, query, static_cast<size_t>(e->d) * 4);
   const ResultLayout L = result_layout(static_cast<size_t>(k), 4);
+  e->launches = 0;
   if (!e->host_graph[k]) {
     if (rbf_status s = capture_host_search(e, k, L)) return s;
   } else {
@@ -734,6 +744,7 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
     if (inject(e, 2)) return RBF_ERR_CUDA;
     e->last_lists = e->host_graph_lists[k];
     e->last_k = k;
+    e->launches = e->host_graph_launches[k];
   }
   const cudaError_t st = cudaGraphLaunch(e->host_graph[k], e->stream);
   if (st != cudaSuccess) return cuda_fail(e, st);
@@ -888,6 +899,7 @@ rbf_status search_resident_batch_dev(rbf_engine* e, const float* d_queries, int3
   if (rbf_status s = sync_view(e)) return s;
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
+  e->launches = 0;
   return enqueue_batch(e, d_queries, b, k, d_idx, d_score, reinterpret_cast<int*>(e->result));
 }
 
@@ -898,6 +910,7 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (!e->ready) return RBF_ERR_NOT_READY;
   if (rbf_status s = check_k(e, k)) return s;
   const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
+  e->launches = 0;
   std::memcpy(e->h_query, queries, qbytes);
   RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
   const size_t count = static_cast<size_t>(b) * k;
@@ -994,6 +1007,7 @@ rbf_status topk_int32_dev(rbf_engine* e, const int32_t* d_data, int64_t n, int32
                           int64_t* d_pos) {
   if (rbf_status s = check_i32_args(e, d_data, n, k)) return s;
   if (!d_val || !d_pos) return RBF_ERR_INVALID_VALUE;
+  e->launches = 0;
   return enqueue_topk_int32(e, d_data, n, k, d_val, d_pos, reinterpret_cast<int*>(e->result));
 }
 
@@ -1002,6 +1016,7 @@ rbf_status topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k
   if (rbf_status s = check_i32_args(e, d_data, n, k)) return s;
   if (!out_val || !out_pos) return RBF_ERR_INVALID_VALUE;
   const ResultLayout L = result_layout(static_cast<size_t>(k), 8);
+  e->launches = 0;
   if (rbf_status s = enqueue_topk_int32(e, d_data, n, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
                                         reinterpret_cast<int64_t*>(e->d_hres + L.b_off),
                                         reinterpret_cast<int*>(e->d_hres)))

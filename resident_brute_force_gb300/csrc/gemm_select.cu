@@ -711,7 +711,9 @@ template <int KP, bool TF32>
 cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tc, const Params& p, int grid, cudaStream_t st) {
   auto fn = gemm_select_pair_kernel<KP, TF32>;
   const int smem = pair_smem_bytes();
-  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce once;
+  const cudaError_t limit =
+      once.run([fn, smem] { return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
   if (limit != cudaSuccess) return limit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));

@@ -79,9 +79,12 @@ cudaError_t launch_t(Params p, int queries, cudaStream_t stream) {
   const int smem =
       std::max(WARPS * KP * 8 + stage_lists * p.k * 8, fast_smem_bytes(p.lists, p.k, p.stage_keys));
   p.smem_bytes = smem;
-  // The largest launch of this instance, set once (thread-safe static).
-  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                        WARPS * KP * 8 + kStageBytes + (kSurvivorCap + 2) * 8);
+  // The largest launch of this instance, set once per device.
+  static PerDeviceOnce once;
+  const cudaError_t limit = once.run([fn] {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                WARPS * KP * 8 + kStageBytes + (kSurvivorCap + 2) * 8);
+  });
   if (limit != cudaSuccess) return limit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(queries));

@@ -9,10 +9,14 @@
 // allocation may take. Such callers cannot create an engine (rbf_create
 // allocates everything up front), but they still want the int32 top-K.
 //
-// topk_int32_noalloc runs the same two kernels as topk_int32_dev and gives the
-// same result. The only scratch those kernels need, one candidate list per
+// topk_int32_noalloc gives the same result as topk_int32_dev. It always runs
+// the register-load stage-1 kernel followed by the merge kernel, the pair the
+// engine uses for arrays under 262,144 elements (the engine switches to its
+// bulk-copy stream kernel from that size on; this entry point does not, as
+// that kernel's bounded waits report through an error word that only an
+// engine has). The only scratch these two kernels need, one candidate list per
 // stage-1 CTA, lives in a fixed array in this library's own device memory,
-// created when the library's device code is loaded.
+// committed when the library's device code is loaded on a device.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -78,7 +82,8 @@ extern "C" rbf_status topk_int32_noalloc(const int32_t* d_data, int64_t n, int32
   DeviceSetup s;
   if (rbf_status st = device_setup(dev, &s)) return st;
 
-  // Same launch shape as topk_int32_dev, clamped to the lists the array holds.
+  // The launch shape topk_int32_dev gives this kernel pair (two CTAs per SM,
+  // at least 8,192 elements each), clamped to the lists the array holds.
   const int64_t per_cta = 8192;
   int64_t grid = std::min<int64_t>(int64_t(s.num_sms) * 2, (n + per_cta - 1) / per_cta);
   grid = std::max<int64_t>(1, std::min<int64_t>(grid, kNoallocMaxLists));
@@ -91,6 +96,9 @@ extern "C" rbf_status topk_int32_noalloc(const int32_t* d_data, int64_t n, int32
   a.partials = s.lists;  // every list is written in full before it is read
   a.partials_cap = static_cast<size_t>(kNoallocMaxLists) * kNoallocListWidth;
   a.grid = static_cast<int>(grid);
+  // No error word: in a checked build a skipped out-of-range store would go
+  // unreported here (the list capacity above is exact, so none can occur).
+  a.err = nullptr;
   if (launch_topk_i32_stage1(a, stream) != cudaSuccess) return RBF_ERR_CUDA;
 
   MergeLaunch m;

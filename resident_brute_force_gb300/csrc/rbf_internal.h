@@ -2,7 +2,9 @@
 // translation units. Not part of the public ABI (that is include/rbf.h).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 namespace rbf {
@@ -12,17 +14,41 @@ constexpr int kScoreConsumerWarps = 8;
 // Warps of the int32 stage-1 kernel.
 constexpr int kI32Warps = 16;
 
-// The current device's opt-in dynamic shared-memory limit per block (read
-// once).
+// The current device's opt-in dynamic shared-memory limit per block.
 inline int max_dynamic_smem() {
-  static const int v = [] {
-    int dev = 0, bytes = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&bytes, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    return bytes;
-  }();
-  return v;
+  int dev = 0, bytes = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&bytes, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return bytes;
 }
+
+// Runs a set-up step once per device, with that device current. A kernel's
+// function attributes (its dynamic shared-memory limit) belong to the device
+// that was current when they were set, so a process that launches on several
+// devices must set them on each. One instance per kernel instance, kept as a
+// function-local static at the launch site; after the first call on a device
+// the cost is a cudaGetDevice and an atomic load.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t st = cudaGetDevice(&dev);
+    if (st != cudaSuccess) return st;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    st = setup();
+    if (st == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return st;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::atomic<bool> done_[kMaxDevices] = {};
+  std::mutex mu_;
+};
 
 // Candidate-list width for a K: the smallest power of two >= max(K, 32).
 inline int list_width(int k) {

@@ -351,14 +351,15 @@ cudaError_t launch_t(const Params& p, int grid, int smem, cudaStream_t stream) {
   auto fn = score_select_f32_kernel<KP, NCH, NORM>;
   // The launch size depends on the engine's options (at most the device's
   // opt-in limit less the kernel's static shared memory), so the limit is
-  // raised once to that maximum (thread-safe static).
-  static const cudaError_t limit = [fn] {
+  // raised to that maximum, once per device.
+  static PerDeviceOnce once;
+  const cudaError_t limit = once.run([fn] {
     cudaFuncAttributes fa;
     const cudaError_t e = cudaFuncGetAttributes(&fa, fn);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 max_dynamic_smem() - static_cast<int>(fa.sharedSizeBytes));
-  }();
+  });
   if (limit != cudaSuccess) return limit;
   fn<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();

@@ -482,7 +482,9 @@ constexpr int kStreamSmem = kSStages * kSTileBytes + kSStages * 32 + kSW * stati
 template <int KP>
 cudaError_t launch_stream_t(const StreamParams& p, int grid, cudaStream_t stream) {
   auto fn = topk_i32_stream_kernel<KP>;
-  static const cudaError_t limit = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem);
+  static PerDeviceOnce once;
+  const cudaError_t limit =
+      once.run([fn] { return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem); });
   if (limit != cudaSuccess) return limit;
   fn<<<grid, kSThreads, kStreamSmem, stream>>>(p);
   return cudaGetLastError();

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def test_bench_line_has_the_contract_keys():
     steps, warmup = 20, 3
     cmd = [sys.executable, "bench.py", "--steps", str(steps), "--warmup", str(warmup), "--n", "100000",
-           "--queries", "64", "--no-batched", "--no-int32", "--no-views", "--no-cosine"]
+           "--queries", "64", "--no-batched", "--no-int32", "--no-views", "--no-cosine", "--no-sweep"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -42,4 +42,11 @@ def test_bench_line_has_the_contract_keys():
     e2e = rec["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] == 1024 * 4 and e2e["d2h_bytes_per_step"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(rec["clocks"])
+    assert rec["clocks"]["samples"] >= 1
+    assert {"headline.k8", "e2e.k8", "config1.l2", "config1.flushed", "config1.e2e"} <= set(rec["clocks"]["regions"])
     assert rec["device"]["name"]
+    c1 = rec["config1"]
+    assert c1["queries"] == 16 and c1["oracle_checked_queries"] == 16 and c1["launches_per_call"] == 1
+    for key in ("p50_us", "p99_us", "flushed_p50_us", "e2e_p50_us"):
+        assert c1[key] > 0, key
+    assert rec["per_k"]["8"]["launches_per_step"] == 1

@@ -291,6 +291,25 @@ def test_sweep_cells_sampled(rbf):
                     check_float_topk(idx, sc, sigma, k)
 
 
+@pytest.mark.parametrize("d", [384, 768, 1024])
+def test_sweep_cells_full_size(rbf, d):
+    """The sweep's two largest row counts (500k and 1M) at every D of the
+    sweep, in the launch shape the bench uses: one sampled query per cell
+    against the oracle at K = 8, 32 and 100 (1M x 1024 is also the planted
+    configuration below)."""
+    n_max = 1_000_000
+    full = workloads.unit_corpus(n_max, d, seed=1)
+    qs = workloads.unit_queries(2, d, seed=2)
+    with make_engine(rbf, n_max, d) as e:
+        for n, q in ((500_000, qs[0]), (1_000_000, qs[1])):
+            c = full[:n]
+            e.upload_corpus_rowmajor(c)
+            sigma = oracle.scores(c, q)
+            for k in (8, 32, 100):
+                idx, sc = e.search_resident(q, k)
+                check_float_topk(idx, sc, sigma, k)
+
+
 def test_full_size_planted(rbf):
     """1,000,000 x 1024 fp32 unit-norm corpus with 10 planted near-duplicates
     per query: full oracle comparison on a sample of queries and the planted

@@ -88,3 +88,7 @@ def test_reference_arm_single_rank_line():
     assert cpu["kind"] == "oracle" and cpu["value"] == rec["value"] and cpu["cores"] >= 1 and cpu["sample"]
     assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
+    # The same configuration as the GPU arm's line, key for key.
+    sys.path.insert(0, ROOT)
+    import bench
+    assert rec["config"] == bench.headline_config(bench.parse([]), 1)

@@ -1,12 +1,14 @@
 """topk_int32_noalloc: the int32 top-K for callers that may not allocate
 device memory (for example a plugin whose GPU memory all comes from its host
-application's allocator). Checked through the C ABI against the engine's
-topk_int32 on two calls in a row. This file is collected last on purpose."""
+application's allocator). Called through the C ABI twice in a row per case and
+checked bit for bit against the oracle and against the engine's topk_int32.
+This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -17,25 +19,29 @@ def _call(lib, d, n, k, dv, dp, stream):
                                   ctypes.c_void_p(dp.data_ptr()), ctypes.c_void_p(stream))
 
 
-def test_noalloc_matches_engine_on_two_calls():
+def test_noalloc_matches_oracle_and_engine_on_two_calls():
     import torch
 
     import resident_brute_force_gb300 as rbf
     lib = rbf.load_library()
     stream = torch.cuda.current_stream().cuda_stream
+    # (n, start offset in elements, K): a ragged size with an unaligned start,
+    # the full 1e8 workload, and a small array with the largest K.
     cases = [(3_000_001, 1, 50), (100_000_000, 0, 20), (777, 3, 256)]
     with rbf.Engine(16, 16, 256) as e:
         for n, offset, k in cases:
             x = workloads.int32_uniform(n + offset, seed=n)
+            o_val, o_pos = oracle.topk_int32(x[offset:], k)
             d = torch.from_numpy(x).cuda()[offset:]
-            ref_val, ref_pos = e.topk_int32(d, k)
+            e_val, e_pos = e.topk_int32(d, k)
             for _ in range(2):
                 dv = torch.full((k,), -1, dtype=torch.int32, device="cuda")
                 dp = torch.full((k,), -1, dtype=torch.int64, device="cuda")
                 assert _call(lib, d, n, k, dv, dp, stream) == rbf.RBF_OK
                 torch.cuda.synchronize()
-                assert np.array_equal(dv.cpu().numpy(), ref_val)
-                assert np.array_equal(dp.cpu().numpy(), ref_pos)
+                got_val, got_pos = dv.cpu().numpy(), dp.cpu().numpy()
+                assert np.array_equal(got_val, o_val) and np.array_equal(got_pos, o_pos), (n, k)
+                assert np.array_equal(got_val, e_val) and np.array_equal(got_pos, e_pos), (n, k)
 
 
 def test_noalloc_rejects_oversized_k():
