@@ -775,6 +775,83 @@ def run_sweep(rbf, clocks, queries):
             "cells": cells}
 
 
+# ------------------------------------------------------------- row shards
+
+def run_sharded(rbf, args, rank: int, world: int) -> dict:
+    """The step on `world` ranks: each rank holds args.n rows (weak
+    scaling: a corpus of world * args.n rows), a step is one sharded search
+    (local search, exchange, merge). value = all ranks' rows x D x 4 bytes per
+    step / the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    from resident_brute_force_gb300.sharded import ShardedSearch
+    n_total, d, nq = args.n * world, args.d, args.queries
+    s = ShardedSearch(rbf, n_total, d, 256, world, rank)
+    shard = workloads.unit_corpus_rows(s.row0, s.rows, d, seed=1)
+    qs = workloads.unit_queries(nq, d, seed=2)
+    planted = workloads.plant_near_duplicates_shard(shard, s.row0, n_total, qs, per_query=10, noise=0.05, seed=3)
+    s.upload(shard)
+    del shard
+    dq = torch.from_numpy(qs).cuda()
+    di = torch.empty(256, dtype=torch.int32, device="cuda")
+    ds = torch.empty(256, dtype=torch.float32, device="cuda")
+    if not args.no_gate:
+        for j in range(0, nq, max(1, nq // 20)):
+            idx, _ = s.search(qs[j], 32)
+            assert set(idx[:10].tolist()) == set(planted[j].tolist()), f"planted rows missing for query {j}"
+    per_k = {}
+    headline = None
+    ks = [8] + [int(x) for x in args.extra_k.split(",") if x]
+    for k in ks:
+        for j in range(args.warmup):
+            s.search_dev(dq[j % nq], k, di, ds)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        dist.barrier()
+        torch.cuda.synchronize()
+        for j in range(args.steps):
+            ev[j].record(s.stream)
+            s.search_dev(dq[j % nq], k, di, ds)
+        ev[args.steps].record(s.stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        step_ms = [ev[j].elapsed_time(ev[j + 1]) for j in range(args.steps)]
+        total_ms = max_over_ranks(ev[0].elapsed_time(ev[args.steps]), world)
+        per_k[str(k)] = {"p50_us": round(percentile(step_ms, 50) * 1e3, 2),
+                         "p99_us": round(percentile(step_ms, 99) * 1e3, 2),
+                         "gbs": round(world * args.steps * args.n * d * 4 / (total_ms * 1e-3) / 1e9, 1),
+                         "launch_us_mean": round(statistics.mean(step_ms) * 1e3, 2)}
+        if k == 8:
+            headline = total_ms
+    for j in range(args.warmup):
+        s.search(qs[j % nq], 8)
+    dist.barrier()
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        s.search(qs[j % nq], 8)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    s.close()
+    value = world * args.steps * args.n * d * 4 / (headline * 1e-3) / 1e9
+    peak, src = hbm_peak()
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(headline / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(headline_config(args, world), n=n_total, rows_per_rank=args.n),
+        "per_k": per_k, "p50_us": per_k["8"]["p50_us"],
+        "roofline": {"kernel": "score_select_f32 (per rank)", "bound": "hbm",
+                     "achieved": round(value / world, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
+                     "frac": round(value / world / peak, 4), "traffic": None},
+        "cpu_baseline": None,
+        "e2e": {"value": round(world * args.steps * args.n * d * 4 / e2e_s / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": d * 4, "d2h_bytes_per_step": 8 * 8},
+        # Per step and rank: the scoring kernel, the shard-list encoding and
+        # the merge kernel (the collective's own kernels are NCCL's).
+        "gpu_launches": 3 * args.steps,
+    }
+
+
 # ------------------------------------------------------------ profiling cases
 
 def run_case(part: str) -> int:
@@ -870,8 +947,7 @@ def main(argv=None):
     if rbf._build.is_stale():
         rbf._build.build()
     if world > 1:
-        from resident_brute_force_gb300 import sharded
-        line = sharded.bench_sharded(rbf, args, rank, world, local)
+        line = run_sharded(rbf, args, rank, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
         import torch.distributed as dist

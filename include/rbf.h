@@ -169,6 +169,20 @@ rbf_status rbf_check_device_error(rbf_engine* engine);
  * view). */
 rbf_status upload_corpus_rowmajor(rbf_engine* engine, const float* corpus, int64_t n, int32_t d);
 
+/* Row shard of a larger corpus: as upload_corpus_rowmajor, for the rows
+ * [row_offset, row_offset + n) of a row-major corpus too large for one
+ * engine (GPU-Resident Top-K for Agentic RAG, section 4 step 1 and section
+ * 9: past one GPU's memory the corpus is split across GPUs). Every search
+ * call of the engine (and of its views) then reports global row indices,
+ * local row + row_offset, and breaks exact score ties by the global index, so
+ * that merge_shard_topk_dev over the shards' results gives exactly what one
+ * engine holding the whole corpus would. upload_corpus_rowmajor is this call
+ * with row_offset 0.
+ *   row_offset  0 .. 2^31-1 - n (global indices must fit in int32)
+ * Errors: those of upload_corpus_rowmajor, INVALID_VALUE (row_offset out of
+ * range). */
+rbf_status upload_corpus_shard(rbf_engine* engine, const float* corpus, int64_t n, int32_t d, int64_t row_offset);
+
 /* ---------------------------------------------------------- single query */
 
 /* Top-K of one query against the resident corpus (the article's
@@ -228,6 +242,35 @@ rbf_status search_resident_batch(rbf_engine* engine, const float* queries, int32
 /* As search_resident_batch with device queries and outputs, stream-ordered. */
 rbf_status search_resident_batch_dev(rbf_engine* engine, const float* d_queries, int32_t b,
                                      int32_t k, int32_t* d_idx, float* d_score);
+
+/* ------------------------------------------------------- row shards */
+
+/* Merge the results of g row shards into the global top-K of each of b
+ * queries: the article's merge step (section 4 step 4) applied across GPUs
+ * instead of across CTAs, after the exchange of every shard's K best
+ * (section 9 lists sharding across GPUs as the way past one GPU's memory).
+ * Each shard's list is what search_resident(_dev) or search_resident_batch
+ * (_dev) returned on an engine loaded with upload_corpus_shard (global
+ * indices, best-first); entries with a negative index are missing (a shard
+ * with fewer than K rows) and rank last. The shards must be disjoint row
+ * ranges, so that no index appears twice. The result is best-first under the
+ * ordering rule; if the shards hold fewer than K rows in all, the last
+ * entries are index -1 with a NaN score.
+ *   d_idx      device, [g][b][k] int32: shard s's list for query q at
+ *              (s * b + q) * k (the layout an all-gather of every shard's
+ *              [b][k] result produces)
+ *   d_score    device, [g][b][k] fp32, the matching scores
+ *   g          1 .. 1024 shards
+ *   b          1 .. max_batch queries
+ *   k          1 .. max_k
+ *   d_out_idx  device, [b][k] int32
+ *   d_out_score device, [b][k] fp32
+ * Stream-ordered on the engine's stream (two launches: the lists become
+ * keys in the engine's partials buffer, then the merge kernel); needs no
+ * resident corpus. Errors: INVALID_VALUE, UNSUPPORTED (b * g * list width
+ * beyond the partials buffer), CUDA. */
+rbf_status merge_shard_topk_dev(rbf_engine* engine, const int32_t* d_idx, const float* d_score, int32_t g,
+                                int32_t b, int32_t k, int32_t* d_out_idx, float* d_out_score);
 
 /* ---------------------------------------------------------- flat int32 */
 

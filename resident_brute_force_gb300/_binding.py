@@ -59,6 +59,8 @@ SIGNATURES = {
     "rbf_last_launches": (_I32, [_P]),
     "rbf_check_device_error": (_S, [_P]),
     "upload_corpus_rowmajor": (_S, [_P, _P, _I64, _I32]),
+    "upload_corpus_shard": (_S, [_P, _P, _I64, _I32, _I64]),
+    "merge_shard_topk_dev": (_S, [_P, _P, _P, _I32, _I32, _I32, _P, _P]),
     "search_resident": (_S, [_P, _P, _I32, _P, _P]),
     "search_resident_dev": (_S, [_P, _P, _I32, _P, _P]),
     "score_select_partials_dev": (_S, [_P, _P, _I32]),
@@ -274,6 +276,17 @@ class Engine:
         self._n, self._d = int(n), int(d)
         del keep
 
+    def upload_corpus_shard(self, corpus, row_offset: int) -> None:
+        """Rows [row_offset, row_offset + N) of a larger corpus: results report
+        global row indices (upload_corpus_shard)."""
+        _need(len(corpus.shape) == 2, "the corpus is a 2-D [N, D] array")
+        keep, ptr = _any_ptr(corpus, np.float32, "float32")
+        n, d = corpus.shape
+        self._check(self.lib.upload_corpus_shard(self._h, ptr, int(n), int(d), int(row_offset)),
+                    "upload_corpus_shard")
+        self._n, self._d = int(n), int(d)
+        del keep
+
     # -- single query
     def search_resident(self, query, k: int):
         q, qp = _host_ptr(np.asarray(query).reshape(-1), np.float32)
@@ -324,6 +337,21 @@ class Engine:
         self._check(self.lib.search_resident_batch_dev(self._h, _dev_ptr(d_queries, "float32"), int(b), int(k),
                                                        _dev_ptr(d_idx, "int32"), _dev_ptr(d_score, "float32")),
                     "search_resident_batch_dev")
+
+    # -- row shards
+    def merge_shard_topk_dev(self, d_idx, d_score, k: int, d_out_idx, d_out_score) -> None:
+        """Merge g shards' best-first lists, d_idx / d_score of shape [g, b, k]
+        (or [g, k] for one query), into [b, k] (merge_shard_topk_dev)."""
+        _need(d_idx.dim() in (2, 3) and tuple(d_idx.shape) == tuple(d_score.shape),
+              "d_idx and d_score are [g, k] or [g, b, k] tensors of one shape")
+        g = d_idx.shape[0]
+        b = d_idx.shape[1] if d_idx.dim() == 3 else 1
+        _need(d_idx.shape[-1] == int(k), f"the lists hold {d_idx.shape[-1]} entries, k = {k}")
+        self._out_len(d_out_idx, b * int(k), "d_out_idx")
+        self._out_len(d_out_score, b * int(k), "d_out_score")
+        self._check(self.lib.merge_shard_topk_dev(self._h, _dev_ptr(d_idx, "int32"), _dev_ptr(d_score, "float32"),
+                                                  int(g), int(b), int(k), _dev_ptr(d_out_idx, "int32"),
+                                                  _dev_ptr(d_out_score, "float32")), "merge_shard_topk_dev")
 
     # -- flat int32
     def topk_int32(self, d_data, k: int):

@@ -35,6 +35,7 @@ constexpr int64_t kSampleRows = 16384;  // rows of the batched path's threshold 
 constexpr int64_t kI32StreamMin = 262144;   // int32 arrays at least this long take the stream kernel
 constexpr int kI32SampleMinK = 65;          // from this K on, the stream kernel also gets a sample bound
 constexpr int64_t kI32SampleElems = 65536;  // elements of that sample
+constexpr int kMaxShards = 1024;            // lists one shard merge takes per query
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -57,6 +58,7 @@ struct rbf_engine {
   int64_t n = 0;
   int d = 0;
   int pitch = 0;
+  int64_t row_offset = 0;  // global index of the first resident row (row shards)
   bool ready = false;
 
   // bf16 copies for the batched path (RBF_FLAG_BF16_CORPUS).
@@ -231,6 +233,7 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_
   // Cosine mode: rows are unit length already; the kernel scales its copy of
   // the query to unit length, so the inner product is the cosine.
   a.normalize_query = (e->flags & RBF_FLAG_COSINE) ? 1 : 0;
+  a.index_offset = static_cast<uint32_t>(e->row_offset);
   const bool fuse = d_idx && score_select_can_merge(e->pitch, k, sh.rows_per_stage, sh.stages);
   if (fuse) {
     a.out_idx = d_idx;
@@ -387,6 +390,7 @@ rbf_status sync_view(rbf_engine* e) {
   e->d = o->d;
   e->pitch = o->pitch;
   e->pitch_bf16 = o->pitch_bf16;
+  e->row_offset = o->row_offset;
   e->last_lists = 0;
   e->last_k = 0;
   e->tmaps_ready = false;
@@ -607,7 +611,12 @@ rbf_status rbf_check_device_error(rbf_engine* e) {
 }
 
 rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n, int32_t d) {
+  return upload_corpus_shard(e, corpus, n, d, 0);
+}
+
+rbf_status upload_corpus_shard(rbf_engine* e, const float* corpus, int64_t n, int32_t d, int64_t row_offset) {
   if (!e || !corpus || n < 1 || n > e->max_n || d < 1 || d > e->max_d || e->owner) return RBF_ERR_INVALID_VALUE;
+  if (row_offset < 0 || row_offset > int64_t(INT32_MAX) - n) return RBF_ERR_INVALID_VALUE;
   if (!e->corpus) return RBF_ERR_UNSUPPORTED;
   e->ready = false;
   ++e->corpus_version;  // views re-read the corpus state at their next call
@@ -651,6 +660,7 @@ rbf_status upload_corpus_rowmajor(rbf_engine* e, const float* corpus, int64_t n,
   e->n = n;
   e->d = d;
   e->pitch = pitch;
+  e->row_offset = row_offset;
   e->ready = true;
   e->last_lists = 0;
   e->last_k = 0;
@@ -806,6 +816,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     // streaming (after the bound merge, or another group, the queries are
     // long complete).
     a.wait_inputs = wait_inputs ? 1 : 0;
+    a.index_offset = static_cast<uint32_t>(e->row_offset);
     RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
     return RBF_OK;
   };
@@ -921,6 +932,32 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (rbf_status s = finish_host_call(e, L)) return s;
   std::memcpy(out_idx, e->h_result + L.a_off, 4 * count);
   std::memcpy(out_score, e->h_result + L.b_off, 4 * count);
+  return RBF_OK;
+}
+
+rbf_status merge_shard_topk_dev(rbf_engine* e, const int32_t* d_idx, const float* d_score, int32_t g, int32_t b,
+                                int32_t k, int32_t* d_out_idx, float* d_out_score) {
+  if (!e || !d_idx || !d_score || !d_out_idx || !d_out_score) return RBF_ERR_INVALID_VALUE;
+  if (g < 1 || g > kMaxShards || b < 1 || b > e->max_batch || k < 1 || k > e->max_k) return RBF_ERR_INVALID_VALUE;
+  const int kp = list_width(k);
+  if (static_cast<size_t>(b) * g * kp > e->partials_cap) return RBF_ERR_UNSUPPORTED;
+  e->launches = 0;
+  e->last_lists = 0;  // the partials buffer is reused: a pending two-step merge is void
+  RBF_LAUNCH(e, launch_encode_shard_lists(d_idx, d_score, g, b, k, kp, e->partials, e->num_sms, e->stream));
+  MergeLaunch m;
+  m.partials = e->partials;
+  m.lists = g;
+  m.queries = b;
+  m.k = k;
+  m.int_keys = 0;
+  m.out_a = d_out_idx;
+  m.out_b = d_out_score;
+  m.err_call = e->errw;
+  m.err_sticky = e->errw + 1;
+  m.result_err = reinterpret_cast<int*>(e->result);
+  m.partials_cap = device_cap(e);
+  m.stride = kp;
+  RBF_LAUNCH(e, launch_merge(m, e->stream));
   return RBF_OK;
 }
 

@@ -208,6 +208,7 @@ struct Params {
   size_t partials_cap;     // keys, lens entries and theta0 entries, for checked builds
   size_t lens_cap;         // (0: not checked)
   size_t theta_cap;
+  uint32_t index_offset;   // added to every row index (global rows of a shard)
 };
 
 // ------------------------------------------------ CTA pairs (2 SMs)
@@ -626,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) eq |= (j < nvalid && sc[j] == mx) ? (1u << j) : 0u;
                 const int jm = eq ? __ffs(eq) - 1 : 0;
-                best[hh * 2 + c2] = umax64(best[hh * 2 + c2], make_key(mx, static_cast<uint32_t>(rb + jm)));
+                best[hh * 2 + c2] =
+                    umax64(best[hh * 2 + c2], make_key(mx, static_cast<uint32_t>(rb + jm) + p.index_offset));
               }
               continue;
             }
@@ -642,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = __ffs(u) - 1;
             u &= u - 1;
             if (m & (1u << j)) {
-              const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j));
+              const uint64_t key = make_key(pick(sc, j), static_cast<uint32_t>(rb + j) + p.index_offset);
               if (key > theta) {
                 cand[cnt * 256 + slot] = key;
                 ++cnt;
@@ -871,6 +873,7 @@ cudaError_t launch_gemm_select(const GemmSelectLaunch& a, cudaStream_t stream) {
   p.partials_cap = a.partials_cap;
   p.lens_cap = a.lens_cap;
   p.theta_cap = a.theta_cap;
+  p.index_offset = a.index_offset;
   const CUtensorMap& tq = *static_cast<const CUtensorMap*>(a.tmap_q);
   const CUtensorMap& tc = *static_cast<const CUtensorMap*>(a.tmap_c);
   return a.tf32 ? launch_typed<true>(tq, tc, p, a, stream) : launch_typed<false>(tq, tc, p, a, stream);

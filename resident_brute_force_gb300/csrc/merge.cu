@@ -99,7 +99,43 @@ cudaError_t launch_t(Params p, int queries, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+// Row-sharded search (GPU-Resident Top-K for Agentic RAG, section 4 step 1
+// and section 9: a corpus beyond one GPU is split into row shards): each
+// shard's best-first (global index, score) list of one query becomes a list
+// of keys with the same ordering rule, so that the merge kernel can combine
+// the shards' lists like the per-CTA lists of one search. Output slot
+// [q][s][e] takes input [s][q][e]; missing entries (index < 0) and the
+// slots from k to kp are the empty key.
+__global__ void encode_shard_lists_kernel(const int32_t* __restrict__ idx, const float* __restrict__ score, int g,
+                                          int b, int k, int kp, uint64_t* __restrict__ out) {
+  pdl_launch_dependents();  // the merge may be scheduled now; it waits for these keys
+  const int64_t total = static_cast<int64_t>(b) * g * kp;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int e = static_cast<int>(i % kp);
+    const int64_t r = i / kp;
+    const int s = static_cast<int>(r % g);
+    const int64_t q = r / g;
+    uint64_t key = 0;
+    if (e < k) {
+      const int64_t src = (static_cast<int64_t>(s) * b + q) * k + e;
+      const int32_t ix = idx[src];
+      if (ix >= 0) key = make_key(score[src], static_cast<uint32_t>(ix));
+    }
+    out[i] = key;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_encode_shard_lists(const int32_t* idx, const float* score, int g, int b, int k, int kp,
+                                      uint64_t* out, int num_sms, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(b) * g * kp;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms) * 8);
+  encode_shard_lists_kernel<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, stream>>>(idx, score, g,
+                                                                                                     b, k, kp, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   Params p;

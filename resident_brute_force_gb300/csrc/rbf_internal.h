@@ -74,6 +74,7 @@ struct ScoreSelectLaunch {
   int dynamic;             // 0 = static contiguous row ranges, 1 = tile claims
   uint64_t timeout_ns;
   int normalize_query = 0; // 1: score with the query scaled to unit length (cosine mode)
+  uint32_t index_offset = 0;  // added to every row index (a row shard's first global row)
   // Set: the last CTA merges the lists into K indices / scores (device or
   // mapped host memory) and hands the error word to result_err / err_sticky.
   int32_t* out_idx = nullptr;
@@ -107,6 +108,13 @@ struct MergeLaunch {
   int short_lists = 0;          // 1: lists hold few valid keys (K > 32): stage a 32-key prefix of each
 };
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
+
+// Row-sharded search: the best-first (index, score) lists of g shards for b
+// queries, laid out [g][b][k] (index < 0: no entry), become keys in
+// out[b][g][kp] (kp >= k; slots past k and missing entries hold the empty
+// key), ready for launch_merge with g lists per query and stride kp.
+cudaError_t launch_encode_shard_lists(const int32_t* idx, const float* score, int g, int b, int k, int kp,
+                                      uint64_t* out, int num_sms, cudaStream_t stream);
 
 struct I32Launch {
   const int32_t* data;
@@ -183,6 +191,7 @@ struct GemmSelectLaunch {
   size_t partials_cap = 0;   // keys in partials, lens entries, theta0 entries: for checked builds
   size_t lens_cap = 0;       // (0: not checked)
   size_t theta_cap = 0;
+  uint32_t index_offset = 0; // added to every row index (a row shard's first global row)
 };
 // Tensor map over a [rows][pitch] bf16 matrix: 64 x 128 boxes, 128-byte swizzle.
 bool make_bf16_tensor_map(void* map, const void* base, int64_t rows, int pitch_elems);

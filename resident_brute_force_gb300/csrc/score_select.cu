@@ -63,6 +63,7 @@ struct Params {
   int* err_sticky;
   int* result_err;
   size_t partials_cap;  // keys (checked builds; 0: not checked)
+  uint32_t index_offset;  // added to every row index (global rows of a shard)
 };
 
 // NCH > 0: rows are exactly NCH * 128 floats and the query lives in
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
         acc += __shfl_xor_sync(kFullMask, acc, 4);
         acc += __shfl_xor_sync(kFullMask, acc, 2);
         acc += __shfl_xor_sync(kFullMask, acc, 1);
-        const uint64_t key = make_key(acc, static_cast<uint32_t>(row0 + r));
+        const uint64_t key = make_key(acc, static_cast<uint32_t>(row0 + r) + p.index_offset);
         if (key > theta) {  // warp-uniform: every lane holds the same acc
           if (lane == cnt) cand = key;
           if (++cnt == 32) {
@@ -422,6 +423,7 @@ cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream)
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;
   p.partials_cap = a.partials_cap;
+  p.index_offset = a.index_offset;
   const int smem = score_select_smem_bytes(a.pitch, a.k, a.rows_per_stage, a.stages);
   switch (list_width(a.k)) {
     case 32: return launch_kp<32>(p, a.grid, smem, a.normalize_query != 0, stream);

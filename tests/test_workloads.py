@@ -61,3 +61,18 @@ def test_planted_rows_are_distinct_and_lead():
         assert np.all(np.abs(planted - expect) < 0.1)
         others = np.delete(scores[:, j], pos.reshape(-1))
         assert planted.min() > others.max()
+
+
+def test_row_ranges_match_the_whole_corpus():
+    """A shard generated on its own has the whole corpus's bytes in its range,
+    and shard planting plants exactly what whole-corpus planting plants there."""
+    full = workloads.unit_corpus(30_000, 40, seed=1)
+    for r0, n in [(0, 30_000), (5, 100), (8190, 10), (8000, 17_000), (29_999, 1), (16_384, 8192)]:
+        assert np.array_equal(workloads.unit_corpus_rows(r0, n, 40, seed=1), full[r0:r0 + n]), (r0, n)
+    qs = workloads.unit_queries(7, 40, seed=2)
+    whole = full.copy()
+    pos = workloads.plant_near_duplicates(whole, qs, per_query=10, noise=0.05, seed=3)
+    for r0, n in [(0, 12_000), (12_000, 18_000), (1000, 20_000)]:
+        part = full[r0:r0 + n].copy()
+        pos_s = workloads.plant_near_duplicates_shard(part, r0, 30_000, qs, per_query=10, noise=0.05, seed=3)
+        assert np.array_equal(pos_s, pos) and np.array_equal(part, whole[r0:r0 + n])

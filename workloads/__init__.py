@@ -74,6 +74,32 @@ def unit_corpus(n: int, d: int, seed: int = 1) -> np.ndarray:
     return gaussian_rows(n, d, seed, STREAM_CORPUS)
 
 
+def unit_corpus_rows(row0: int, n: int, d: int, seed: int = 1) -> np.ndarray:
+    """Rows [row0, row0 + n) of the unit-norm Gaussian corpus of any size
+    larger than row0 + n: the same bytes as unit_corpus(N, d, seed)[row0:row0 + n]
+    (block b of rows always draws from its own stream, and a short last block
+    draws a prefix of the same sequence), without generating the other rows.
+    This is how one row shard of a corpus too large for one GPU is made."""
+    out = np.empty((n, d), dtype=np.float32)
+    b0 = row0 // BLOCK_ROWS
+    b1 = (row0 + n + BLOCK_ROWS - 1) // BLOCK_ROWS
+
+    def fill(i: int) -> None:
+        b = b0 + i
+        lo = max(row0, b * BLOCK_ROWS)
+        hi = min(row0 + n, (b + 1) * BLOCK_ROWS)
+        if hi <= lo:
+            return
+        g = _rng(seed, STREAM_CORPUS, b).standard_normal((hi - b * BLOCK_ROWS, d))[lo - b * BLOCK_ROWS:]
+        norms = np.sqrt(np.einsum("ij,ij->i", g, g))
+        norms[norms == 0.0] = 1.0
+        g /= norms[:, None]
+        out[lo - row0:hi - row0] = g
+
+    _parallel(fill, b1 - b0)
+    return out
+
+
 def unit_queries(b: int, d: int, seed: int = 2) -> np.ndarray:
     """Unit-norm Gaussian queries: the corpus distribution under seed+1."""
     return gaussian_rows(b, d, seed, STREAM_QUERY)
@@ -87,8 +113,28 @@ def plant_near_duplicates(corpus: np.ndarray, queries: np.ndarray, per_query: in
 
     Modifies ``corpus`` in place.
     """
-    n, d = corpus.shape
-    nq = queries.shape[0]
+    n = corpus.shape[0]
+    pos, rows = _planted(n, queries, per_query, noise, seed)
+    corpus[pos.reshape(-1)] = rows
+    return pos
+
+
+def plant_near_duplicates_shard(shard: np.ndarray, row0: int, n_total: int, queries: np.ndarray,
+                                per_query: int = 10, noise: float = 0.05, seed: int = 3) -> np.ndarray:
+    """plant_near_duplicates on a corpus of n_total rows of which ``shard``
+    holds rows [row0, row0 + len(shard)): the rows planted there are the ones
+    the whole-corpus call would plant in that range. Returns every planted
+    global row index, shape (len(queries), per_query). Modifies ``shard``."""
+    pos, rows = _planted(n_total, queries, per_query, noise, seed)
+    flat = pos.reshape(-1)
+    mine = (flat >= row0) & (flat < row0 + shard.shape[0])
+    shard[flat[mine] - row0] = rows[mine]
+    return pos
+
+
+def _planted(n: int, queries: np.ndarray, per_query: int, noise: float, seed: int):
+    """Planted positions (nq, per_query) over n rows and the planted rows (nq * per_query, d), fp32."""
+    nq, d = queries.shape
     total = nq * per_query
     if total > n:
         raise ValueError("more planted rows than corpus rows")
@@ -97,8 +143,7 @@ def plant_near_duplicates(corpus: np.ndarray, queries: np.ndarray, per_query: in
     g = _rng(seed, STREAM_PLANT_NOISE, 0).standard_normal((total, d))
     rows = queries.astype(np.float64).repeat(per_query, axis=0) + noise * g
     rows /= np.sqrt(np.einsum("ij,ij->i", rows, rows))[:, None]
-    corpus[pos.reshape(-1)] = rows.astype(np.float32)
-    return pos
+    return pos, rows.astype(np.float32)
 
 
 def int32_uniform(n: int, seed: int = 1) -> np.ndarray:
