@@ -73,6 +73,8 @@ def parse(argv=None):
     ap.add_argument("--no-views", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-config1", action="store_true")
+    ap.add_argument("--sharded", action="store_true",
+                    help="run the row-sharded step (local search, all-gather, merge) even on one rank")
     ap.add_argument("--schedule", type=int, default=None)
     ap.add_argument("--ctas-per-sm", type=int, default=None)
     ap.add_argument("--stage-bytes", type=int, default=None)
@@ -437,14 +439,30 @@ def percentile(xs, p):
     return s[i]
 
 
+HOST_AHEAD_S_PER_CALL = 40e-6  # host time to enqueue one call (Python binding + launch), generous
+
+
+def hold_stream(stream, calls):
+    """Keep `stream` busy (a GPU spin kernel, outside every timed event) for
+    longer than the host needs to enqueue `calls` calls, so that the timed
+    calls then run back to back on the device: device time per call, not the
+    host's issue rate."""
+    import torch
+    cycles = int(2.2e9 * max(1e-3, calls * HOST_AHEAD_S_PER_CALL))
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(cycles)
+
+
 def time_device(stream, fn, steps, warmup):
-    """Per-call device times (ms) of fn() on `stream`, events at call boundaries."""
+    """Per-call device times (ms) of fn() on `stream`, events at call boundaries,
+    with the calls enqueued ahead of the device (hold_stream)."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             fn()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     torch.cuda.synchronize()
+    hold_stream(stream, steps)
     with torch.cuda.stream(stream):
         for j in range(steps):
             ev[j].record(stream)
@@ -463,6 +481,7 @@ def time_device_flushed(stream, fn, steps, warmup, flush):
             fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
+    hold_stream(stream, 2 * steps)
     with torch.cuda.stream(stream):
         for j in range(steps):
             flush.fill_(j & 0xFF)
@@ -938,15 +957,19 @@ def main(argv=None):
     import torch
 
     rank, world, local = dist_env()
-    if world > 1:
+    sharded = world > 1 or args.sharded
+    if sharded:
         import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29531")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", rank=rank, world_size=world)
     torch.cuda.set_device(local)
 
     import resident_brute_force_gb300 as rbf
     if rbf._build.is_stale():
         rbf._build.build()
-    if world > 1:
+    if sharded:
         line = run_sharded(rbf, args, rank, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -996,6 +1019,7 @@ def main(argv=None):
         # at every step boundary on the launching stream time each launch.
         bounds = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         torch.cuda.synchronize()
+        hold_stream(stream, args.steps)
         with clocks.region(f"headline.k{k}"):
             with torch.cuda.stream(stream):
                 for j in range(args.steps):

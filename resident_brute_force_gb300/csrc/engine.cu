@@ -820,8 +820,10 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     RBF_LAUNCH(e, launch_gemm_select(a, e->stream));
     return RBF_OK;
   };
-  // All groups of up to 256 queries over rows [0, rows), lists of 32 keys;
-  // returns the number of per-CTA lists per query.
+  // All groups of up to 256 queries over rows [0, rows); returns the number
+  // of lists per query: in bound mode one per CTA and column half (4 keys
+  // each), else one per CTA pair (32 keys each: the pair's two column halves
+  // are merged in the kernel).
   auto score_groups = [&](int64_t rows, int bound_mode, const uint64_t* theta0, int* lists) -> rbf_status {
     const int grid = grid_for(rows);
     if (static_cast<size_t>(b) * grid * kBatchListWidth > e->partials_cap) return RBF_ERR_UNSUPPORTED;
@@ -831,7 +833,7 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
                                        q0 == 0 && (bound_mode || theta0 == nullptr)))
         return st;
     }
-    *lists = grid;
+    *lists = bound_mode ? grid : grid / 2;
     return RBF_OK;
   };
   // Pre-pass over the first S rows: no selection, each per-CTA list of a
@@ -863,8 +865,8 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
     m.result_err = nullptr;
     m.partials_cap = device_cap(e);
     m.kth_out = e->theta0;
-    m.stride = kBatchListWidth;
-    m.short_lists = k > kBatchRegMaxK ? 1 : 0;  // 4 chunk maxima per list
+    m.stride = kBoundListWidth;  // 4 chunk maxima per list
+    m.short_lists = k > kBatchRegMaxK ? 1 : 0;
     RBF_LAUNCH(e, launch_merge(m, e->stream));
     theta0 = e->theta0;
   }

@@ -5,7 +5,7 @@
 // runs on the 5th-generation tensor cores (tcgen05): bf16 inputs, fp32
 // accumulators in tensor memory (TMEM). The selection is the same problem as
 // the single-query path (GPU-Resident Top-K for Agentic RAG, section 4 steps
-// 3-4: per-block partial top-K, then a merge): every CTA leaves one
+// 3-4: per-block partial top-K, then a merge): every CTA pair leaves one
 // best-first list per query, and the merge kernel finishes each query.
 //
 // One kernel, gemm_select_pair_kernel: clusters of two CTAs, one CTA per
@@ -27,7 +27,9 @@
 //              best, buffers their keys 16 deep in shared memory and merges
 //              full buffers into its best-first list: KP <= 32 keys in
 //              registers, or for K > 32 a list in global memory (the
-//              thread's slot of the partials buffer) with its length.
+//              thread's slot of the partials buffer) with its length. At
+//              the end the two warps on the same lanes merge their K <= 32
+//              lists, so a query gets one list per CTA pair.
 // The scores never reach memory: each thread writes one list per query. In
 // bound mode (the pre-pass over a row sample) it writes instead the best key
 // of each of its four 32-column chunks, folded over its tiles.
@@ -147,6 +149,22 @@ __device__ __forceinline__ void list_merge8(uint64_t (&L)[KP], const uint64_t (&
   }
 }
 
+// Sort a bitonic sequence of KP keys in registers into descending order.
+template <int KP>
+__device__ __forceinline__ void bitonic_clean_desc(uint64_t (&L)[KP]) {
+#pragma unroll
+  for (int j = KP / 2; j > 0; j >>= 1) {
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+      if ((i & j) == 0) {
+        const uint64_t a = L[i], b = L[i + j];
+        L[i] = umax64(a, b);
+        L[i + j] = umin64(a, b);
+      }
+    }
+  }
+}
+
 template <int KP>
 __device__ __forceinline__ uint64_t list_get(const uint64_t (&L)[KP], int e) {
   uint64_t x = 0;
@@ -192,7 +210,8 @@ __device__ __forceinline__ float pick(const float (&sc)[32], int j) {
 }
 
 struct Params {
-  uint64_t* partials;  // [queries][grid][32] keys; K > 32: [queries][grid][KP], lens[queries][grid] long
+  uint64_t* partials;  // [queries][grid / 2][32] keys; K > 32: [queries][grid][KP], lens[queries][grid] long;
+                       // bound mode: [queries][grid][4]
   int* err;
   int64_t n;           // corpus rows
   int kchunks;         // 128-byte K chunks per row (64 bf16 or 32 fp32 elements)
@@ -230,6 +249,9 @@ constexpr int kPairStages = 6;
 constexpr int kPairStageBytes = 2 * kSubTileBytes;  // A (own 128 queries) | B (own 128 rows)
 constexpr int kPairTileRows = 256;
 constexpr int kPairAccArrivals = 2 * kEpiWarps;     // epilogue warps of both CTAs
+// At the end the idle ring holds the epilogue warps' list transposes and the
+// column-half list exchange.
+static_assert(kPairStages * kPairStageBytes >= (kEpiWarps * 32 * 33 + 4 * 32 * 32) * 8, "ring too small");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -667,17 +689,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       cswap(best[0], best[2]);
       cswap(best[1], best[3]);
       cswap(best[1], best[2]);
-      // Every MMA of the pair has finished (the last accumulator was full),
-      // so this CTA's ring is free for the transposed list write.
-      store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane,
-                    live ? p.partials + list_id() * 32 : nullptr, [&](int i) { return i < 4 ? best[i] : 0ull; });
+      // Lists of kBoundListWidth (4) keys: two 16-byte stores per thread.
+      if (live) {
+        ulonglong2* dst = reinterpret_cast<ulonglong2*>(p.partials + list_id() * kBoundListWidth);
+        dst[0] = make_ulonglong2(best[0], best[1]);
+        dst[1] = make_ulonglong2(best[2], best[3]);
+      }
     } else {
       if (__any_sync(kFullMask, cnt > 0)) merge_buffer();
       if constexpr (kWide) {
         if (live) p.lens[list_id()] = len;
       } else {
-        store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane,
-                      live ? p.partials + list_id() * 32 : nullptr, [&](int i) { return i < KP ? L[i] : 0ull; });
+        // The two warps on the same TMEM lanes (column halves h = 0 and 1)
+        // hold two lists per query. The h = 1 warp hands its list over
+        // through shared memory (every MMA has finished, so the ring is
+        // idle), and the h = 0 warp folds it into its own (reversed max, then
+        // a bitonic merge) and writes one list per query and CTA pair.
+        uint64_t* xch = reinterpret_cast<uint64_t*>(ring) + kEpiWarps * (32 * 33) + quad * (32 * KP);
+        if (h == 1) {
+#pragma unroll
+          for (int i = 0; i < KP; ++i) xch[i * 32 + lane] = L[i];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        if (h == 0) {
+#pragma unroll
+          for (int i = 0; i < KP; ++i) L[KP - 1 - i] = umax64(L[KP - 1 - i], xch[i * 32 + lane]);
+          bitonic_clean_desc<KP>(L);
+          const size_t pair_list = static_cast<size_t>(p.q_out0 + qidx) * nclusters + cluster;
+          store_lists32(reinterpret_cast<uint64_t*>(ring) + e * (32 * 33), lane,
+                        live ? p.partials + pair_list * 32 : nullptr, [&](int i) { return i < KP ? L[i] : 0ull; });
+        }
       }
     }
   }

@@ -165,12 +165,14 @@ cudaError_t launch_normalize_queries_bf16(const float* src, int64_t src_pitch, v
 constexpr int kBatchRegMaxK = 32;  // batched K up to this: per-thread lists in registers
 constexpr int kBatchQueriesPerLaunch = 256;
 constexpr int kBatchListWidth = 32;
+constexpr int kBoundListWidth = 4;  // bound pre-pass: 4 chunk maxima per (query, CTA, column half)
 constexpr int kBf16PitchAlign = 64;  // bf16 elements: one 128-byte swizzle row
 
 struct GemmSelectLaunch {
   const void* tmap_q;        // host CUtensorMap over the bf16 query buffer
   const void* tmap_c;        // host CUtensorMap over the bf16 corpus
-  uint64_t* partials;        // [queries][grid][32] keys; K > 32: [queries][grid][list_width(K)]
+  uint64_t* partials;        // [queries][grid / 2][32] keys (one list per CTA pair); K > 32:
+                             // [queries][grid][list_width(K)]; bound mode: [queries][grid][4]
   int* err;
   int64_t n;                 // corpus rows
   int kchunks;               // 128-byte K chunks per row (64 bf16 or 32 fp32 elements each)
@@ -179,12 +181,12 @@ struct GemmSelectLaunch {
   int q_count;               // queries in this launch, 1..256
   int q_out0;                // first query of this launch in the partials layout
   int k;
-  int grid;                  // even: 2 x min(ceil(n / 256), SMs / 2); also the lists per query
+  int grid;                  // even: 2 x min(ceil(n / 256), SMs / 2)
   uint64_t timeout_ns;
   const uint64_t* theta0;    // optional per-query lower bound on the K-th key (keys >= it are kept)
   int bound_mode = 0;        // 1: no selection; each list (query, CTA, column half) holds the best key
                              // of each of 4 chunks of its rows (chunk c: columns 32c..32c+31 of its
-                             // half of each tile), best first, then zeros
+                             // half of each tile), best first: kBoundListWidth keys per list
   int* lens = nullptr;       // K > 32: [queries][grid] valid keys of each list (required)
   int wait_inputs = 1;       // 1: the kernel launched just before wrote the queries (the producer waits
                              // for it); 0: the corpus stream may start while that kernel finishes
