@@ -453,9 +453,12 @@ def hold_stream(stream, calls):
         torch.cuda._sleep(cycles)
 
 
-def time_device(stream, fn, steps, warmup):
+def time_device(stream, fn, steps, warmup, back_to_back=False):
     """Per-call device times (ms) of fn() on `stream`, events at call boundaries,
-    with the calls enqueued ahead of the device (hold_stream)."""
+    with the calls enqueued ahead of the device (hold_stream). With
+    back_to_back, also the mean per call (ms) of a second pass of `steps`
+    calls with events only at its two ends: an event record between two
+    launches costs ~2 us of device time, which matters for short calls."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -469,7 +472,18 @@ def time_device(stream, fn, steps, warmup):
             fn()
         ev[steps].record(stream)
     torch.cuda.synchronize()
-    return [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
+    per_call = [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
+    if not back_to_back:
+        return per_call
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(stream, steps)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return per_call, a.elapsed_time(b) / steps
 
 
 def time_device_flushed(stream, fn, steps, warmup, flush):
@@ -532,7 +546,8 @@ def run_batched(rbf, clocks, steps, warmup, tf32=False):
     ds = torch.empty((b, k), dtype=torch.float32, device="cuda")
     tag = "batched_tf32" if tf32 else "batched"
     with clocks.region(f"{tag}.k32"):
-        ms = time_device(st, lambda: e.search_resident_batch_dev(dq, k, di, ds), steps, warmup)
+        ms, mean = time_device(st, lambda: e.search_resident_batch_dev(dq, k, di, ds), steps, warmup,
+                               back_to_back=True)
     launches = e.last_launches
     # The other K buckets: 8 (register lists, like 32) and 100 (per-thread
     # lists in the partials buffer, one merge per 256-query group).
@@ -568,7 +583,7 @@ def run_batched(rbf, clocks, steps, warmup, tf32=False):
             "tensor_frac": round(flops / p50 / 1e12 / peak, 4),
             "corpus_gbs": round(corpus_bytes / p50 / 1e9, 1), "hbm_peak_gbs": hbm, "hbm_peak_source": hsrc,
             "hbm_frac": round(corpus_bytes / p50 / 1e9 / hbm, 4), "bound": bound,
-            "queries_per_s": round(b / p50, 1),
+            "queries_per_s": round(b / p50, 1), "mean_us_back_to_back": round(mean * 1e3, 1),
             "k8_p50_us": round(percentile(other[8], 50) * 1e3, 1),
             "k100_p50_us": round(percentile(other[100], 50) * 1e3, 1),
             "b16_p50_us": round(percentile(ms16, 50) * 1e3, 1),
@@ -669,12 +684,14 @@ def run_int32(rbf, clocks, steps, warmup):
     hbm, _ = hbm_peak()
     for k in (20, 50):
         with clocks.region(f"int32.k{k}"):
-            ms = time_device(st, lambda: e.topk_int32_dev(x, k, dv, dp), steps, warmup)
+            ms, mean = time_device(st, lambda: e.topk_int32_dev(x, k, dv, dp), steps, warmup, back_to_back=True)
         with clocks.region(f"int32.k{k}.e2e"):
             host = time_host(lambda: e.topk_int32(x, k), steps, 3)
         p50 = percentile(ms, 50) * 1e-3
         out[f"k{k}"] = {"p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(ms, 99) * 1e3, 1),
                         "gbs": round(4.0 * n / p50 / 1e9, 1), "hbm_frac": round(4.0 * n / p50 / 1e9 / hbm, 4),
+                        "mean_us_back_to_back": round(mean * 1e3, 1),
+                        "hbm_frac_back_to_back": round(4.0 * n / (mean * 1e-3) / 1e9 / hbm, 4),
                         "e2e_p50_us": round(percentile(host, 50) * 1e6, 1),
                         "e2e_p99_us": round(percentile(host, 99) * 1e6, 1),
                         "e2e_d2h_bytes_per_call": result_d2h_bytes(k, 8)}
@@ -715,7 +732,8 @@ def run_config1(rbf, clocks, reps):
     steps = nq * reps
     it = iter(range(10 ** 9))
     with clocks.region("config1.l2"):
-        warm = time_device(st, lambda: e.search_resident_dev(dq[next(it) % nq], k, di, ds), steps, 20)
+        warm, warm_mean = time_device(st, lambda: e.search_resident_dev(dq[next(it) % nq], k, di, ds), steps, 20,
+                                      back_to_back=True)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     with clocks.region("config1.flushed"):
         cold = time_device_flushed(st, lambda: e.search_resident_dev(dq[next(it) % nq], k, di, ds), steps, 20,
@@ -732,6 +750,7 @@ def run_config1(rbf, clocks, reps):
             "queries": nq, "calls": steps, "l2": "corpus 15.4 MB < L2: L2-resident unless flushed",
             "p50_us": round(p50 * 1e6, 2), "p99_us": round(percentile(warm, 99) * 1e3, 2),
             "qps": round(1.0 / p50, 1), "gbs_l2": round(n * d * 4 / p50 / 1e9, 1),
+            "mean_us_back_to_back": round(warm_mean * 1e3, 2),
             "flushed_p50_us": round(p50c * 1e6, 2), "flushed_p99_us": round(percentile(cold, 99) * 1e3, 2),
             "flushed_gbs": round(n * d * 4 / p50c / 1e9, 1),
             "flushed_hbm_frac": round(n * d * 4 / p50c / 1e9 / hbm, 4),
@@ -773,8 +792,8 @@ def run_sweep(rbf, clocks, queries):
                 dsc = torch.empty(k, dtype=torch.float32, device="cuda")
                 it = iter(range(10 ** 9))
                 with clocks.region(f"sweep.n{n}.d{d}.k{k}"):
-                    dev = time_device(st, lambda: eng.search_resident_dev(dq[next(it) % queries], k, di, dsc),
-                                      queries, 10)
+                    dev, b2b = time_device(st, lambda: eng.search_resident_dev(dq[next(it) % queries], k, di, dsc),
+                                           queries, 10, back_to_back=True)
                     it2 = iter(range(10 ** 9))
                     host = time_host(lambda: eng.search_resident(qs[next(it2) % queries], k), queries, 10)
                 p50 = percentile(dev, 50) * 1e-3
@@ -782,6 +801,7 @@ def run_sweep(rbf, clocks, queries):
                 cells.append({
                     "n": n, "d": d, "k": k, "queries": queries,
                     "p50_us": round(p50 * 1e6, 1), "p99_us": round(percentile(dev, 99) * 1e3, 1),
+                    "mean_us_back_to_back": round(b2b * 1e3, 1),
                     "qps": round(1.0 / mean, 1), "gbs": round(nbytes / mean / 1e9, 1),
                     "hbm_frac": round(nbytes / mean / 1e9 / hbm, 4),
                     "e2e_p50_us": round(percentile(host, 50) * 1e6, 1),
@@ -1015,27 +1035,39 @@ def main(argv=None):
             for j in range(args.warmup):
                 eng.search_resident_dev(dq[j % nq], k, d_idx, d_sc)
         # One step is one search_resident_dev call: a single launch of the
-        # scoring kernel, whose last CTA also merges the per-CTA lists. Events
-        # at every step boundary on the launching stream time each launch.
+        # scoring kernel, whose last CTA also merges the per-CTA lists. The
+        # timed region is exactly `steps` back-to-back calls between two events
+        # on the launching stream (throughput, mean launch duration); a second
+        # pass with an event at every step boundary gives the per-call p50/p99.
+        qv = [dq[j % nq] for j in range(args.steps)]
+        t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         bounds = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         torch.cuda.synchronize()
-        hold_stream(stream, args.steps)
         with clocks.region(f"headline.k{k}"):
+            hold_stream(stream, args.steps)
+            with torch.cuda.stream(stream):
+                t_a.record(stream)
+                for j in range(args.steps):
+                    eng.search_resident_dev(qv[j], k, d_idx, d_sc)
+                t_b.record(stream)
+            torch.cuda.synchronize()
+            hold_stream(stream, args.steps)
             with torch.cuda.stream(stream):
                 for j in range(args.steps):
                     bounds[j].record(stream)
-                    eng.search_resident_dev(dq[j % nq], k, d_idx, d_sc)
+                    eng.search_resident_dev(qv[j], k, d_idx, d_sc)
                 bounds[args.steps].record(stream)
             torch.cuda.synchronize()
         step_ms = [bounds[j].elapsed_time(bounds[j + 1]) for j in range(args.steps)]
-        total_ms = bounds[0].elapsed_time(bounds[args.steps])
+        total_ms = t_a.elapsed_time(t_b)
         launches_per_step = eng.last_launches
         rec = {
             "p50_us": round(percentile(step_ms, 50) * 1e3, 2),
             "p99_us": round(percentile(step_ms, 99) * 1e3, 2),
             "gbs": round(args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9, 1),
             "qps": round(args.steps / (total_ms * 1e-3), 1),
-            "launch_us_mean": round(statistics.mean(step_ms) * 1e3, 2),
+            "launch_us_mean": round(total_ms / args.steps * 1e3, 2),
+            "per_call_event_us_mean": round(statistics.mean(step_ms) * 1e3, 2),
             "launches_per_step": launches_per_step,
         }
         per_k[str(k)] = rec
@@ -1065,8 +1097,9 @@ def main(argv=None):
     total_ms, step_ms = headline
     value = args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
-    # The dominant (only) kernel's average launch duration: the mean step.
-    k1_mean_s = statistics.mean(step_ms) * 1e-3
+    # The dominant (only) kernel's average launch duration: the mean step of
+    # the timed back-to-back region.
+    k1_mean_s = total_ms / args.steps * 1e-3
     achieved = bytes_per_step / k1_mean_s / 1e9
     roofline = {"kernel": "score_select_f32", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),

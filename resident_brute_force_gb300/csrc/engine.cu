@@ -76,7 +76,6 @@ struct rbf_engine {
   bool tmaps_ready = false;
 
   // Workspaces (device).
-  float* query = nullptr;        // max_batch * max_pitch floats
   uint64_t* partials = nullptr;  // partials_cap keys
   uint64_t* i32_theta0 = nullptr;  // int32 path: K-th key of the element sample
   size_t partials_cap = 0;
@@ -316,7 +315,6 @@ void release(rbf_engine* e) {
   cudaFree(e->query_f32);
   cudaFree(e->theta0);
   cudaFree(e->lens);
-  cudaFree(e->query);
   cudaFree(e->partials);
   cudaFree(e->errw);
   cudaFree(e->counters);
@@ -346,7 +344,6 @@ rbf_status alloc_call_buffers(rbf_engine* e) {
   ok = ok && cudaMalloc(&e->theta0, static_cast<size_t>(e->max_batch) * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->lens, static_cast<size_t>(kBatchQueriesPerLaunch) * e->num_sms * sizeof(int)) ==
                  cudaSuccess;
-  ok = ok && cudaMalloc(&e->query, static_cast<size_t>(e->max_batch) * e->max_pitch * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->partials, e->partials_cap * sizeof(uint64_t)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->errw, 4 * sizeof(int)) == cudaSuccess;
   ok = ok && cudaMalloc(&e->counters, 8 * sizeof(unsigned)) == cudaSuccess;
@@ -365,8 +362,6 @@ rbf_status alloc_call_buffers(rbf_engine* e) {
   }
   ok = cudaMemsetAsync(e->errw, 0, 4 * sizeof(int), e->stream) == cudaSuccess &&
        cudaMemsetAsync(e->counters, 0, 8 * sizeof(unsigned), e->stream) == cudaSuccess &&
-       cudaMemsetAsync(e->query, 0, static_cast<size_t>(e->max_batch) * e->max_pitch * sizeof(float), e->stream) ==
-           cudaSuccess &&
        cudaStreamSynchronize(e->stream) == cudaSuccess;
   if (!ok) {
     release(e);
@@ -838,8 +833,8 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   };
   // Pre-pass over the first S rows: no selection, each per-CTA list of a
   // query holds the best key of each of 4 chunks of the rows it covers, and
-  // the merge takes the K-th largest of those chunk maxima (4 per list, 512
-  // at S = 16,384). K distinct rows score at least that much, so it is a lower
+  // a small kernel takes the K-th largest of those chunk maxima (4 per list,
+  // 512 at S = 16,384). K distinct rows score at least that much, so it is a lower
   // bound on the final K-th key, and the main pass drops every key below it.
   // About K * N / S keys pass it; above K = 32 each one costs a merge into a
   // list in global memory, so S grows with K (16,384 per 32 of K), up to a
@@ -852,22 +847,29 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   if (sample_rows >= 256) {
     int lists = 0;
     if (rbf_status st = score_groups(sample_rows, 1, nullptr, &lists)) return st;
-    MergeLaunch m;
-    m.partials = e->partials;
-    m.lists = lists;
-    m.queries = b;
-    m.k = k;
-    m.int_keys = 0;
-    m.out_a = d_idx;  // overwritten by the final merge
-    m.out_b = d_score;
-    m.err_call = nullptr;
-    m.err_sticky = nullptr;
-    m.result_err = nullptr;
-    m.partials_cap = device_cap(e);
-    m.kth_out = e->theta0;
-    m.stride = kBoundListWidth;  // 4 chunk maxima per list
-    m.short_lists = k > kBatchRegMaxK ? 1 : 0;
-    RBF_LAUNCH(e, launch_merge(m, e->stream));
+    const int total = lists * kBoundListWidth;  // chunk maxima per query, contiguous
+    if (total <= RBF_KTH_MAX_KEYS) {
+      RBF_LAUNCH(e, launch_kth_of_lists(e->partials, b, total, k, e->theta0, e->stream));
+    } else {
+      // More lists than the bound kernel takes (a device with more than 256
+      // SMs): the merge kernel gives the same K-th key.
+      MergeLaunch m;
+      m.partials = e->partials;
+      m.lists = lists;
+      m.queries = b;
+      m.k = k;
+      m.int_keys = 0;
+      m.out_a = d_idx;  // overwritten by the final merge
+      m.out_b = d_score;
+      m.err_call = nullptr;
+      m.err_sticky = nullptr;
+      m.result_err = nullptr;
+      m.partials_cap = device_cap(e);
+      m.kth_out = e->theta0;
+      m.stride = kBoundListWidth;  // 4 chunk maxima per list
+      m.short_lists = k > kBatchRegMaxK ? 1 : 0;
+      RBF_LAUNCH(e, launch_merge(m, e->stream));
+    }
     theta0 = e->theta0;
   }
   if (k <= kBatchRegMaxK) {
@@ -924,11 +926,14 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (rbf_status s = check_k(e, k)) return s;
   const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
   e->launches = 0;
+  // The queries go to the device through the pinned staging block, which the
+  // query conversion kernel reads in place (mapped; coherent over NVLink-C2C
+  // on GB300), as the single-query search does: that is the call's copy.
+  if (inject(e, 1)) return RBF_ERR_CUDA;
   std::memcpy(e->h_query, queries, qbytes);
-  RBF_COPY(e, cudaMemcpyAsync(e->query, e->h_query, qbytes, cudaMemcpyHostToDevice, e->stream));
   const size_t count = static_cast<size_t>(b) * k;
   const ResultLayout L = result_layout(count, 4);
-  if (rbf_status s = enqueue_batch(e, e->query, b, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
+  if (rbf_status s = enqueue_batch(e, e->d_hquery, b, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
                                    reinterpret_cast<float*>(e->d_hres + L.b_off), reinterpret_cast<int*>(e->d_hres)))
     return s;
   if (rbf_status s = finish_host_call(e, L)) return s;

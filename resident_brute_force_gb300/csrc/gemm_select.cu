@@ -779,6 +779,7 @@ cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tc, const Pa
 // rows in [rows, rows_total).
 __global__ void to_bf16_kernel(const float* __restrict__ src, int64_t src_pitch, __nv_bfloat16* __restrict__ dst,
                                int64_t dst_pitch, int64_t rows, int64_t rows_total, int cols) {
+  pdl_launch_dependents();  // the scoring pass may become resident now; its producer waits for these queries
   const int64_t total = rows_total * dst_pitch;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {

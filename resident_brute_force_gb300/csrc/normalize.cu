@@ -51,6 +51,7 @@ __global__ void normalize_rows_kernel(float* corpus, int64_t n, int d, int pitch
 __global__ void normalize_queries_bf16_kernel(const float* __restrict__ src, int64_t src_pitch,
                                               __nv_bfloat16* __restrict__ dst, int64_t dst_pitch, int64_t rows,
                                               int64_t rows_total, int cols) {
+  pdl_launch_dependents();  // the scoring pass may become resident now; its producer waits for these queries
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows_total;
@@ -73,6 +74,7 @@ __global__ void normalize_queries_bf16_kernel(const float* __restrict__ src, int
 template <bool NORM>
 __global__ void stage_queries_f32_kernel(const float* __restrict__ src, int64_t src_pitch, float* __restrict__ dst,
                                          int64_t dst_pitch, int64_t rows, int64_t rows_total, int cols) {
+  pdl_launch_dependents();  // the scoring pass may become resident now; its producer waits for these queries
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows_total;

@@ -94,6 +94,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
     }
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: this CTA may become resident while that kernel's last CTA is
+  // still merging. Nothing above touched global memory; everything below
+  // (the query, the tile counters, the lists) waits for that kernel.
+  pdl_wait();
   if constexpr (NCH == 0) {
     for (int i = threadIdx.x; i < p.pitch; i += blockDim.x) sq[i] = (i < p.d) ? p.query[i] : 0.0f;
     if constexpr (NORM) {
@@ -362,8 +367,17 @@ cudaError_t launch_t(const Params& p, int grid, int smem, cudaStream_t stream) {
                                 max_dynamic_smem() - static_cast<int>(fa.sharedSizeBytes));
   });
   if (limit != cudaSuccess) return limit;
-  fn<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 template <int KP, bool NORM>

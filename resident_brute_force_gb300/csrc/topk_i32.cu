@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     }
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent: resident early, but the array, the
+  // counters and the lists are touched only after the previous kernel on the
+  // stream has finished.
+  pdl_wait();
   __syncthreads();
 
   uint64_t v[R];
@@ -486,8 +490,17 @@ cudaError_t launch_stream_t(const StreamParams& p, int grid, cudaStream_t stream
   const cudaError_t limit =
       once.run([fn] { return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem); });
   if (limit != cudaSuccess) return limit;
-  fn<<<grid, kSThreads, kStreamSmem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(kStreamSmem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 // Wait on an mbarrier nothing ever arrives at, through the library's bounded
