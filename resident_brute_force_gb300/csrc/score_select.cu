@@ -84,6 +84,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int RS = p.rows_per_stage;
+  const int64_t total_tiles = (p.n + RS - 1) / RS;
+  // With dynamic claims CTA b's first tile is tile b, issued before the wait
+  // on the previous kernel below: the corpus is never written by a kernel
+  // (an upload synchronises the stream), so the copy may overlap that
+  // kernel's tail. The claims then start at tile gridDim.x.
+  const bool first_early = p.dynamic && blockIdx.x < total_tiles;
   pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for us
 
   if (threadIdx.x == 0) {
@@ -93,6 +99,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
       mbar_init(&empty[s], NW);
     }
     fence_mbar_init();
+    if (first_early) {
+      const int64_t row0 = static_cast<int64_t>(blockIdx.x) * RS;
+      const int rows = static_cast<int>(min(p.n, row0 + RS) - row0);
+      const uint32_t bytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(p.pitch) * 4u;
+      hdr_row0[0] = row0;
+      hdr_rows[0] = rows;
+      mbar_arrive_expect_tx(&full[0], bytes);
+      bulk_copy_g2s(ring, p.corpus + row0 * p.pitch, bytes, &full[0], l2_policy_evict_first());
+    }
   }
   // Launched as a programmatic dependent of the previous kernel on the
   // stream: this CTA may become resident while that kernel's last CTA is
@@ -132,14 +147,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       const int64_t row_bytes = static_cast<int64_t>(p.pitch) * 4;
-      const int64_t total_tiles = (p.n + RS - 1) / RS;
       const int64_t r0 = p.n * blockIdx.x / gridDim.x;
       const int64_t r1 = p.n * (blockIdx.x + 1) / gridDim.x;
       const int64_t local_tiles = (r1 - r0 + RS - 1) / RS;
-      int64_t claim = p.dynamic ? static_cast<int64_t>(atomicAdd(&p.counters[0], 1u)) : 0;
-      int64_t issued = 0;
+      int64_t claim = p.dynamic ? static_cast<int64_t>(atomicAdd(&p.counters[0], 1u)) + gridDim.x : 0;
+      int64_t issued = first_early ? 1 : 0;  // the first tile, issued in the prologue
       bool aborted = false;
-      for (int64_t i = 0;; ++i) {
+      for (int64_t i = issued;; ++i) {
         const int s = static_cast<int>(i % p.stages);
         const uint32_t u = static_cast<uint32_t>(i / p.stages);
         const bool end = p.dynamic ? (claim >= total_tiles) : (i >= local_tiles);
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
           if (p.dynamic) {
             row0 = claim * RS;
             row_end = min(p.n, row0 + RS);
-            claim = static_cast<int64_t>(atomicAdd(&p.counters[0], 1u));  // next claim, in flight
+            claim = static_cast<int64_t>(atomicAdd(&p.counters[0], 1u)) + gridDim.x;  // next claim, in flight
           } else {
             row0 = r0 + i * RS;
             row_end = min(r1, row0 + RS);
