@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -208,7 +209,8 @@ rbf_status check_k(const rbf_engine* e, int k) {
 // also merges the lists into the outputs (one launch per search), else the
 // lists stay for enqueue_merge (last_lists). *merged tells which happened.
 rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_idx = nullptr,
-                         float* d_score = nullptr, int* result_err = nullptr, bool* merged = nullptr) {
+                         float* d_score = nullptr, int* result_err = nullptr, bool* merged = nullptr,
+                         bool host_result = false) {
   ScoreShape sh;
   if (!score_shape(e, k, &sh)) return RBF_ERR_UNSUPPORTED;
   if (static_cast<size_t>(sh.grid) * list_width(k) > e->partials_cap) return RBF_ERR_UNSUPPORTED;
@@ -239,6 +241,7 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_
     a.out_score = d_score;
     a.err_sticky = e->errw + 1;
     a.result_err = result_err;
+    a.host_result = host_result ? 1 : 0;
   }
   RBF_LAUNCH(e, launch_score_select(a, e->stream));
   e->last_lists = sh.grid;
@@ -248,7 +251,7 @@ rbf_status enqueue_score(rbf_engine* e, const float* d_query, int k, int32_t* d_
 }
 
 rbf_status enqueue_merge(rbf_engine* e, int k, int lists, int queries, int int_keys, int32_t* out_a, void* out_b,
-                         int* result_err) {
+                         int* result_err, bool host_result = false) {
   MergeLaunch m;
   m.partials = e->partials;
   m.lists = lists;
@@ -260,6 +263,7 @@ rbf_status enqueue_merge(rbf_engine* e, int k, int lists, int queries, int int_k
   m.err_call = e->errw;
   m.err_sticky = e->errw + 1;
   m.result_err = result_err;
+  m.host_result = host_result && queries == 1 ? 1 : 0;
   m.partials_cap = device_cap(e);
   RBF_LAUNCH(e, launch_merge(m, e->stream));
   return RBF_OK;
@@ -287,6 +291,36 @@ rbf_status finish_host_call(rbf_engine* e, const ResultLayout& L) {
   if (st != cudaSuccess) return cuda_fail(e, st);
   int derr = 0;
   std::memcpy(&derr, e->h_result, sizeof(int));
+  if (derr & kErrBounds) return RBF_ERR_BOUNDS;
+  if (derr != 0) return RBF_ERR_TIMEOUT;
+  return RBF_OK;
+}
+
+// The error word of a one-CTA call's results (a single-query search, an
+// int32 top-K) is written by the device after the results, over the
+// kResultPending mark left here before the launch.
+void mark_result_pending(rbf_engine* e) { reinterpret_cast<volatile int*>(e->h_result)[0] = kResultPending; }
+
+// Wait for such a call by watching its error word in the pinned result block,
+// which lands (over NVLink-C2C on GB300) as soon as the kernel writes it,
+// sooner than a stream synchronisation returns; the stream is queried every
+// 256 reads, so a launch that fails or finishes without writing the word
+// ends the wait too. The results are in place when the word has changed.
+rbf_status finish_host_call_polled(rbf_engine* e) {
+  volatile int* w = reinterpret_cast<volatile int*>(e->h_result);
+  for (unsigned spin = 1; *w == kResultPending; ++spin) {
+    if ((spin & 255u) == 0) {
+      const cudaError_t st = cudaStreamQuery(e->stream);
+      if (st == cudaSuccess) break;
+      if (st != cudaErrorNotReady) return cuda_fail(e, st);
+    }
+  }
+  std::atomic_thread_fence(std::memory_order_acquire);
+  const int derr = *w;
+  if (derr == kResultPending) {  // the stream finished without the word: report it, don't read stale results
+    const cudaError_t st = cudaStreamSynchronize(e->stream);
+    return cuda_fail(e, st != cudaSuccess ? st : cudaErrorUnknown);
+  }
   if (derr & kErrBounds) return RBF_ERR_BOUNDS;
   if (derr != 0) return RBF_ERR_TIMEOUT;
   return RBF_OK;
@@ -703,9 +737,9 @@ static rbf_status enqueue_host_search(rbf_engine* e, int k, const ResultLayout& 
   float* out_score = reinterpret_cast<float*>(e->d_hres + L.b_off);
   int* result_err = reinterpret_cast<int*>(e->d_hres);
   bool merged = false;
-  if (rbf_status s = enqueue_score(e, e->d_hquery, k, out_idx, out_score, result_err, &merged)) return s;
+  if (rbf_status s = enqueue_score(e, e->d_hquery, k, out_idx, out_score, result_err, &merged, true)) return s;
   if (merged) return RBF_OK;
-  return enqueue_merge(e, k, e->last_lists, 1, 0, out_idx, out_score, result_err);
+  return enqueue_merge(e, k, e->last_lists, 1, 0, out_idx, out_score, result_err, true);
 }
 
 // Record enqueue_host_search for this K as a CUDA graph (one launch per
@@ -742,6 +776,7 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
   std::memcpy(e->h_query, query, static_cast<size_t>(e->d) * 4);
   const ResultLayout L = result_layout(static_cast<size_t>(k), 4);
   e->launches = 0;
+  mark_result_pending(e);
   if (!e->host_graph[k]) {
     if (rbf_status s = capture_host_search(e, k, L)) return s;
   } else {
@@ -753,7 +788,7 @@ rbf_status search_resident(rbf_engine* e, const float* query, int32_t k, int32_t
   }
   const cudaError_t st = cudaGraphLaunch(e->host_graph[k], e->stream);
   if (st != cudaSuccess) return cuda_fail(e, st);
-  if (rbf_status s = finish_host_call(e, L)) return s;
+  if (rbf_status s = finish_host_call_polled(e)) return s;
   std::memcpy(out_idx, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
   std::memcpy(out_score, e->h_result + L.b_off, 4 * static_cast<size_t>(k));
   return RBF_OK;
@@ -969,7 +1004,7 @@ rbf_status merge_shard_topk_dev(rbf_engine* e, const int32_t* d_idx, const float
 }
 
 static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k, int32_t* val,
-                                     int64_t* pos, int* result_err) {
+                                     int64_t* pos, int* result_err, bool host_result = false) {
   // Register-load stage 1 over contiguous ranges; below 8,192 elements per
   // CTA fewer CTAs are used.
   auto stage1 = [&](int64_t count, int* lists) -> rbf_status {
@@ -992,7 +1027,7 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
   int lists = 0;
   if (n < kI32StreamMin) {
     if (rbf_status st = stage1(n, &lists)) return st;
-    return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err);
+    return enqueue_merge(e, k, lists, 1, 1, val, pos, result_err, host_result);
   }
   // Large arrays: the bulk-copy ring kernel, one CTA per SM. Each CTA bounds
   // the K-th key from its own slice before its first tile. That bound weakens
@@ -1036,6 +1071,7 @@ static rbf_status enqueue_topk_int32(rbf_engine* e, const int32_t* d_data, int64
   a.out_pos = pos;
   a.err_sticky = e->errw + 1;
   a.result_err = result_err;
+  a.host_result = host_result ? 1 : 0;
   RBF_LAUNCH(e, launch_topk_i32_stream(a, e->stream));
   return RBF_OK;
 }
@@ -1061,11 +1097,12 @@ rbf_status topk_int32(rbf_engine* e, const int32_t* d_data, int64_t n, int32_t k
   if (!out_val || !out_pos) return RBF_ERR_INVALID_VALUE;
   const ResultLayout L = result_layout(static_cast<size_t>(k), 8);
   e->launches = 0;
+  mark_result_pending(e);
   if (rbf_status s = enqueue_topk_int32(e, d_data, n, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
                                         reinterpret_cast<int64_t*>(e->d_hres + L.b_off),
-                                        reinterpret_cast<int*>(e->d_hres)))
+                                        reinterpret_cast<int*>(e->d_hres), true))
     return s;
-  if (rbf_status s = finish_host_call(e, L)) return s;
+  if (rbf_status s = finish_host_call_polled(e)) return s;
   std::memcpy(out_val, e->h_result + L.a_off, 4 * static_cast<size_t>(k));
   std::memcpy(out_pos, e->h_result + L.b_off, 8 * static_cast<size_t>(k));
   return RBF_OK;

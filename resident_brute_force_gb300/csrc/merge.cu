@@ -35,6 +35,7 @@ struct Params {
   const int* lens;    // optional: [query][list] valid keys per list
   int stage_keys;     // shared-memory budget (keys) for staged list heads
   size_t partials_cap;  // keys (checked builds; 0: not checked)
+  int host_result;      // 1: one query, results in mapped host memory, the host waits on result_err
 };
 
 constexpr int kManyQueries = 64;          // from this many queries on, merge CTAs are 8 warps
@@ -62,13 +63,23 @@ __global__ void __launch_bounds__(WARPS * 32, 1) merge_partials_kernel(const Par
   }
   o.err = p.err_sticky ? p.err_sticky : p.err_call;
   mergecore::merge_lists<KP, WARPS * 32>(o, base, p.lists, smem, p.smem_bytes, p.stage_keys);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.err_call) {
-    // Hand the per-call device error word to the host-visible result and
-    // the sticky word, then re-arm it for the next call.
+  if (!p.err_call) return;
+  // Hand the per-call device error word to the sticky word and re-arm it;
+  // the result word follows the results. With one query (one CTA) the word
+  // is published after this CTA's results, so a host caller may wait for
+  // it; with several, only the stream's completion covers every CTA.
+  __shared__ int s_err;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
     const int e = *p.err_call;
-    if (p.result_err) *p.result_err = e;
     if (e && p.err_sticky) atomicOr(p.err_sticky, e);
     *p.err_call = 0;
+    s_err = e;
+  }
+  if (gridDim.x == 1) {
+    __syncthreads();
+    publish_result_word(p.result_err, s_err, p.host_result != 0);
+  } else if (blockIdx.x == 0 && threadIdx.x == 0 && p.result_err) {
+    *p.result_err = s_err;
   }
 }
 
@@ -219,6 +230,7 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream) {
   p.stride = a.stride > 0 ? a.stride : list_width(a.k);
   p.lens = a.lens;
   p.partials_cap = a.partials_cap;
+  p.host_result = a.host_result;
   // Short lists (a prefix of K valid keys, or fewer): stage 32 keys of each
   // (the rest is read from L2 if it survives), so that the CTA's shared
   // memory stays small and all queries run in one wave.

@@ -38,6 +38,29 @@ __device__ __forceinline__ bool in_bounds(bool ok, int* err) {
 __device__ __forceinline__ bool in_bounds(bool, int*) { return true; }
 #endif
 
+// The error word of a call whose results go to the host is written last,
+// over this mark that the host left there before the launch: the host may
+// wait for the word to change instead of synchronising the stream. Real
+// error words are ORs of the kErr bits above.
+constexpr int kResultPending = 0x40000000;
+
+// Publish a one-CTA call's error word after its results. For results in
+// host memory that the host waits on (host_result), every thread's writes
+// reach system scope first; device-memory results need no fence (the stream
+// orders them). Block-uniform.
+__device__ __forceinline__ void publish_result_word(int* result_err, int e, bool host_result) {
+  if (host_result) {
+    __threadfence_system();
+    __syncthreads();
+    if (threadIdx.x == 0 && result_err) {
+      __threadfence_system();
+      *reinterpret_cast<volatile int*>(result_err) = e;
+    }
+  } else if (threadIdx.x == 0 && result_err) {
+    *result_err = e;
+  }
+}
+
 // ----------------------------------------------------------------- keys
 //
 // A key packs (score, index) so that key_a > key_b exactly when a is better

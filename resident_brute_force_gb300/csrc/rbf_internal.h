@@ -81,6 +81,7 @@ struct ScoreSelectLaunch {
   float* out_score = nullptr;
   int* err_sticky = nullptr;
   int* result_err = nullptr;
+  int host_result = 0;      // 1: results in mapped host memory, the host waits on result_err
   size_t partials_cap = 0;  // keys in partials, for checked builds (0: not checked)
 };
 
@@ -101,6 +102,7 @@ struct MergeLaunch {
   int* err_call;             // per-call error word, moved out and cleared
   int* err_sticky;           // sticky error word (ORed)
   int* result_err;           // where the per-call error lands (may be null)
+  int host_result = 0;       // 1: one query, results in mapped host memory, the host waits on result_err
   uint64_t* kth_out = nullptr;  // optional: each query's K-th key
   int stride = 0;               // keys from one list to the next (0: list_width(k))
   const int* lens = nullptr;    // optional [queries x lists] valid keys per list (else all stride)
@@ -155,6 +157,7 @@ struct I32StreamLaunch {
   int64_t* out_pos = nullptr;
   int* err_sticky = nullptr;
   int* result_err = nullptr;
+  int host_result = 0;         // 1: results in mapped host memory, the host waits on result_err
   size_t partials_cap = 0;     // keys in partials, for checked builds (0: not checked)
 };
 cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream);

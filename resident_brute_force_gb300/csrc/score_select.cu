@@ -64,6 +64,7 @@ struct Params {
   int* result_err;
   size_t partials_cap;  // keys (checked builds; 0: not checked)
   uint32_t index_offset;  // added to every row index (global rows of a shard)
+  int host_result;        // 1: results in mapped host memory, the host waits on result_err
 };
 
 // NCH > 0: rows are exactly NCH * 128 floats and the query lives in
@@ -355,14 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_select_f32_kernel(const Par
     // The ring only (the barriers after it are left alone).
     mergecore::merge_lists<KP, kThreads>(o, p.partials, static_cast<int>(gridDim.x), reinterpret_cast<uint64_t*>(smem),
                                          p.region_bytes, merge_stage_keys(p.region_bytes));
+    // Hand the per-call error word to the sticky word and re-arm it for the
+    // next call, then publish it to the result block after the results.
+    __shared__ int s_err;
     if (threadIdx.x == 0) {
-      // Hand the per-call error word to the result block and the sticky
-      // word, then re-arm it for the next call.
       const int e = atomicOr(p.err, 0);
-      if (p.result_err) *p.result_err = e;
       if (e && p.err_sticky) atomicOr(p.err_sticky, e);
       atomicExch(p.err, 0);
+      s_err = e;
     }
+    __syncthreads();
+    publish_result_word(p.result_err, s_err, p.host_result != 0);
   }
 }
 
@@ -452,6 +456,7 @@ cudaError_t launch_score_select(const ScoreSelectLaunch& a, cudaStream_t stream)
   p.result_err = a.result_err;
   p.partials_cap = a.partials_cap;
   p.index_offset = a.index_offset;
+  p.host_result = a.host_result;
   const int smem = score_select_smem_bytes(a.pitch, a.k, a.rows_per_stage, a.stages);
   switch (list_width(a.k)) {
     case 32: return launch_kp<32>(p, a.grid, smem, a.normalize_query != 0, stream);

@@ -224,6 +224,7 @@ struct StreamParams {
   int* err_sticky;
   int* result_err;
   size_t partials_cap;  // keys (checked builds; 0: not checked)
+  int host_result;      // 1: results in mapped host memory, the host waits on result_err
 };
 
 // The last CTA merges in the ring's shared memory (the barriers after it are
@@ -470,14 +471,17 @@ __global__ void __launch_bounds__(kSThreads, 1) topk_i32_stream_kernel(const Str
     o.err = p.err;
     mergecore::merge_lists<KP, kSThreads>(o, p.partials, static_cast<int>(gridDim.x),
                                           reinterpret_cast<uint64_t*>(smem), kMergeSmemBytes, kMergeStageKeys);
+    // Hand the per-call error word to the sticky word and re-arm it, then
+    // publish it to the host-visible result after the results.
+    __shared__ int s_err;
     if (threadIdx.x == 0) {
-      // Hand the per-call error word to the host-visible result and the
-      // sticky word, then re-arm it for the next call.
       const int e = atomicOr(p.err, 0);
-      if (p.result_err) *p.result_err = e;
       if (e && p.err_sticky) atomicOr(p.err_sticky, e);
       atomicExch(p.err, 0);
+      s_err = e;
     }
+    __syncthreads();
+    publish_result_word(p.result_err, s_err, p.host_result != 0);
   }
 }
 
@@ -545,6 +549,7 @@ cudaError_t launch_topk_i32_stream(const I32StreamLaunch& a, cudaStream_t stream
   p.err = a.err;
   p.timeout_ns = a.timeout_ns;
   p.out_val = a.out_val;
+  p.host_result = a.host_result;
   p.out_pos = a.out_pos;
   p.err_sticky = a.err_sticky;
   p.result_err = a.result_err;

@@ -6,6 +6,8 @@ data (exact scores, heavy ties across shard boundaries), within the fp32 rule
 on the 1M x 1024 planted configuration. On several GPUs the lists travel
 through one all-gather instead of a device copy (resident_brute_force_gb300
 .sharded); the kernels are the same."""
+import os
+
 import numpy as np
 import pytest
 
@@ -161,3 +163,49 @@ def test_shard_argument_errors(rbf):
             assert lib.merge_shard_topk_dev(e._h, gi.data_ptr(), gs.data_ptr(), g, b, k, oi.data_ptr(),
                                             osc.data_ptr()) == rbf.RBF_ERR_INVALID_VALUE, (g, b, k)
         assert e.check_device_error() == rbf.RBF_OK
+
+
+_ONE_RANK = r'''
+import os, sys, json
+sys.path.insert(0, os.getcwd())
+import numpy as np, torch, torch.distributed as dist
+import oracle, workloads
+import resident_brute_force_gb300 as rbf
+from resident_brute_force_gb300.sharded import ShardedSearch
+torch.cuda.set_device(0)
+dist.init_process_group("nccl", rank=0, world_size=1)
+n, d = 20_011, 64
+c = workloads.dyadic_grid(n, d, seed=88)
+qs = workloads.dyadic_grid(4, d, seed=89)
+s = ShardedSearch(rbf, n, d, 128, 1, 0)
+s.upload(c[s.row0:s.row0 + s.rows])
+ok = True
+for q in qs:
+    for k in (1, 16, 128):
+        idx, sc = s.search(q, k)
+        o_idx, o_sc = oracle.topk(c, q, k)
+        ok = ok and np.array_equal(idx.astype(np.int64), o_idx) and np.array_equal(sc.astype(np.float64), o_sc)
+s.close()
+dist.destroy_process_group()
+print(json.dumps({"ok": bool(ok)}))
+'''
+
+
+def test_sharded_search_one_rank_nccl(tmp_path):
+    """ShardedSearch end to end in a one-rank NCCL group (its own process):
+    the local search, the all-gather and the merge, bit for bit against the
+    oracle. Several ranks need several GPUs; their host logic is
+    tests/test_sharded_host.py."""
+    import json
+    import socket
+    import subprocess
+    import sys
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), NCCL_NVLS_ENABLE="0")
+    r = subprocess.run([sys.executable, "-c", _ONE_RANK], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert json.loads(r.stdout.strip().splitlines()[-1])["ok"]
