@@ -135,15 +135,39 @@ def _host_ptr(a: np.ndarray, dtype) -> tuple[np.ndarray, int]:
     return a, a.ctypes.data
 
 
+_TORCH_DTYPES: dict = {}
+
+
 def _dev_ptr(t, dtype_name: str) -> int:
     """Device pointer of a contiguous CUDA torch tensor of the given dtype."""
     if not getattr(t, "is_cuda", False):
         raise TypeError("expected a CUDA tensor")
-    if str(t.dtype) != f"torch.{dtype_name}":
+    want = _TORCH_DTYPES.get(dtype_name)
+    if want is None:
+        import torch
+        want = _TORCH_DTYPES.setdefault(dtype_name, getattr(torch, dtype_name))
+    if t.dtype != want:
         raise TypeError(f"expected torch.{dtype_name}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     return t.data_ptr()
+
+
+class _HostBuffers:
+    """An engine's host arrays for its single-query and int32 host-buffer
+    calls, with their addresses taken once: numpy builds a helper object each
+    time an array's address is read (~2 us), while copying a query into a
+    fixed buffer and the K results out of one costs well under that."""
+
+    def __init__(self):
+        self.q = np.empty(RBF_MAX_D, np.float32)
+        self.idx = np.empty(RBF_MAX_K, np.int32)
+        self.sc = np.empty(RBF_MAX_K, np.float32)
+        self.pos = np.empty(RBF_MAX_K, np.int64)
+        self.q_p = self.q.ctypes.data
+        self.idx_p = self.idx.ctypes.data
+        self.sc_p = self.sc.ctypes.data
+        self.pos_p = self.pos.ctypes.data
 
 
 def _need(ok: bool, msg: str) -> None:
@@ -197,11 +221,20 @@ class Engine:
         """Dimension of the resident corpus (None before an upload); a view reports its base's."""
         return self._base.d if self._base is not None else self._d
 
+    def _host_buffers(self) -> _HostBuffers:
+        hb = getattr(self, "_hb", None)
+        if hb is None:
+            hb = self._hb = _HostBuffers()
+        return hb
+
     def _out_len(self, t, count: int, what: str) -> None:
-        _need(t.numel() >= max(int(count), 0), f"{what} holds {t.numel()} entries, the call writes {count}")
+        if t.numel() < count:
+            raise ValueError(f"{what} holds {t.numel()} entries, the call writes {count}")
 
     def _query_len(self, size: int, what: str) -> None:
-        _need(self.d is None or size == self.d, f"{what} has {size} elements, the corpus has D = {self.d}")
+        d = self.d
+        if d is not None and size != d:
+            raise ValueError(f"{what} has {size} elements, the corpus has D = {d}")
 
     def view(self, stream=None) -> "Engine":
         """A second handle on this engine's resident corpus with its own stream
@@ -289,13 +322,17 @@ class Engine:
 
     # -- single query
     def search_resident(self, query, k: int):
-        q, qp = _host_ptr(np.asarray(query).reshape(-1), np.float32)
-        self._query_len(q.size, "the query")
-        idx = np.empty(max(int(k), 0), dtype=np.int32)
-        sc = np.empty(max(int(k), 0), dtype=np.float32)
-        self._check(self.lib.search_resident(self._h, qp, int(k), idx.ctypes.data, sc.ctypes.data),
-                    "search_resident")
-        return idx, sc
+        q = np.asarray(query)
+        if q.ndim != 1:
+            q = q.reshape(-1)
+        self._query_len(q.shape[0], "the query")
+        if q.shape[0] > RBF_MAX_D:
+            raise ValueError(f"the query has {q.shape[0]} elements, more than RBF_MAX_D")
+        hb = self._host_buffers()
+        k = int(k)
+        hb.q[:q.shape[0]] = q  # the library reads D floats from here (cast to float32)
+        self._check(self.lib.search_resident(self._h, hb.q_p, k, hb.idx_p, hb.sc_p), "search_resident")
+        return hb.idx[:k].copy(), hb.sc[:k].copy()
 
     def search_resident_dev(self, d_query, k: int, d_idx, d_score) -> None:
         self._query_len(d_query.numel(), "d_query")
@@ -355,11 +392,11 @@ class Engine:
 
     # -- flat int32
     def topk_int32(self, d_data, k: int):
-        val = np.empty(max(int(k), 0), dtype=np.int32)
-        pos = np.empty(max(int(k), 0), dtype=np.int64)
-        self._check(self.lib.topk_int32(self._h, _dev_ptr(d_data, "int32"), int(d_data.numel()), int(k),
-                                        val.ctypes.data, pos.ctypes.data), "topk_int32")
-        return val, pos
+        hb = self._host_buffers()
+        k = int(k)
+        self._check(self.lib.topk_int32(self._h, _dev_ptr(d_data, "int32"), int(d_data.numel()), k, hb.idx_p,
+                                        hb.pos_p), "topk_int32")
+        return hb.idx[:k].copy(), hb.pos[:k].copy()
 
     def topk_int32_dev(self, d_data, k: int, d_val, d_pos) -> None:
         self._out_len(d_val, k, "d_val")
