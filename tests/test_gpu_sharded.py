@@ -187,7 +187,7 @@ for q in qs:
         ok = ok and np.array_equal(idx.astype(np.int64), o_idx) and np.array_equal(sc.astype(np.float64), o_sc)
 s.close()
 dist.destroy_process_group()
-print(json.dumps({"ok": bool(ok)}))
+print("RESULT " + json.dumps({"ok": bool(ok)}), flush=True)
 '''
 
 
@@ -208,4 +208,7 @@ def test_sharded_search_one_rank_nccl(tmp_path):
     r = subprocess.run([sys.executable, "-c", _ONE_RANK], cwd=root, env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
-    assert json.loads(r.stdout.strip().splitlines()[-1])["ok"]
+    # Libraries may print to stdout too: the result is the line marked RESULT.
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("RESULT ")]
+    assert lines, r.stdout[-2000:] + r.stderr[-2000:]
+    assert json.loads(lines[-1][len("RESULT "):])["ok"]
