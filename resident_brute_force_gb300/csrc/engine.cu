@@ -874,11 +874,19 @@ static rbf_status enqueue_batch(rbf_engine* e, const float* d_queries, int b, in
   // About K * N / S keys pass it; above K = 32 each one costs a merge into a
   // list in global memory, so S grows with K (16,384 per 32 of K), up to a
   // quarter of the corpus.
+  // The default sample is rounded up to whole rounds of 256-row tiles over
+  // every CTA pair (19,456 rows on 152 SMs): the pre-pass then holds every
+  // SM, so the bound kernel's small CTAs land one per SM beside it and leave
+  // room for the main pass's CTAs, instead of stacking up on SMs the
+  // pre-pass left free and keeping main-pass CTAs off them.
   const uint64_t* theta0 = nullptr;
-  const int64_t sample_rows =
-      e->batch_sample < 0
-          ? std::min<int64_t>(kSampleRows * ((k + 31) / 32), e->n / 4 / kSampleRows * kSampleRows)
-          : std::min<int64_t>(e->batch_sample, e->n);
+  int64_t sample_rows = e->batch_sample < 0
+                            ? std::min<int64_t>(kSampleRows * ((k + 31) / 32), e->n / 4 / kSampleRows * kSampleRows)
+                            : std::min<int64_t>(e->batch_sample, e->n);
+  if (e->batch_sample < 0 && sample_rows > 0) {
+    const int64_t round_rows = static_cast<int64_t>(256) * (e->num_sms / 2);
+    sample_rows = std::min<int64_t>((sample_rows + round_rows - 1) / round_rows * round_rows, e->n / 4);
+  }
   if (sample_rows >= 256) {
     int lists = 0;
     if (rbf_status st = score_groups(sample_rows, 1, nullptr, &lists)) return st;

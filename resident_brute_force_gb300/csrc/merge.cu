@@ -137,73 +137,60 @@ __global__ void encode_shard_lists_kernel(const int32_t* __restrict__ idx, const
   }
 }
 
-// The batched path's bound (the K-th largest chunk maximum of each query):
-// one CTA of 8 warps per query over its `total` keys (the pre-pass lists,
-// contiguous per query). Each warp folds up to four 32-key batches into a
-// register top-K list, the eight lists merge pairwise in shared memory, and
-// the K-th key of the result (0 if fewer than K keys are nonzero) is written.
-constexpr int kKthWarps = 8;
-constexpr int kKthMaxKeys = 4 * kKthWarps * 32;
-static_assert(kKthMaxKeys == RBF_KTH_MAX_KEYS, "four 32-key batches per warp");
+// The batched path's bound: one warp per query over its `total` keys (the
+// pre-pass lists, contiguous per query). The warp finds the largest score code
+// c (the key's high word) that at least K of the keys reach, one bit at a time
+// from the top: a bit is kept when K keys still reach the code with it set.
+// K distinct rows then score at least c, so c << 32 (index word zero) bounds
+// the K-th key from below; 0 if fewer than K keys are nonzero. A CTA of two
+// such warps without shared memory fits beside a scoring CTA on its SM, and
+// 128 of them cover 256 queries, one per SM beside the pre-pass: the main
+// pass's CTAs never wait for these to leave.
+constexpr int kKthPerLane = RBF_KTH_MAX_KEYS / 32;
+constexpr int kKthWarpsPerCta = 2;
 
-template <int KP>
-__global__ void __launch_bounds__(kKthWarps * 32) kth_of_lists_kernel(const uint64_t* __restrict__ keys, int total,
-                                                                      int k, uint64_t* __restrict__ kth_out) {
-  constexpr int R = KP / 32;
-  __shared__ __align__(16) uint64_t lists[kKthWarps * KP];
+__global__ void __launch_bounds__(kKthWarpsPerCta * 32) kth_code_kernel(const uint64_t* __restrict__ keys,
+                                                                        int queries, int total, int k,
+                                                                        uint64_t* __restrict__ kth_out) {
   pdl_launch_dependents();  // the main pass may be scheduled now; it waits for the bounds
   pdl_wait();
-  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint64_t* src = keys + static_cast<size_t>(blockIdx.x) * total;
-  uint64_t c[4];
+  const int q = blockIdx.x * kKthWarpsPerCta + (threadIdx.x >> 5);
+  if (q >= queries) return;
+  const uint64_t* src = keys + static_cast<size_t>(q) * total;
+  uint32_t c[kKthPerLane];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = (j * kKthWarps + warp) * 32 + lane;
-    c[j] = i < total ? __ldcg(src + i) : 0ull;
+  for (int j = 0; j < kKthPerLane; ++j) {
+    const int i = j * 32 + lane;
+    c[j] = i < total ? static_cast<uint32_t>(__ldcg(src + i) >> 32) : 0u;
   }
-  uint64_t v[R];
-  warp_list_clear<R>(v);
+  uint32_t res = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t t = res | (1u << bit);
+    unsigned n = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if ((j * kKthWarps + warp) * 32 < total) warp_list_insert32<R>(v, c[j], lane);
-  warp_list_store<R>(v, lists + warp * KP, lane);
-  __syncthreads();
-#pragma unroll
-  for (int step = 1; step < kKthWarps; step <<= 1) {
-    if ((warp % (2 * step)) == 0) {
-      warp_list_merge_from<R>(v, lists + (warp + step) * KP, lane);
-      warp_list_store<R>(v, lists + warp * KP, lane);
-    }
-    __syncthreads();
+    for (int j = 0; j < kKthPerLane; ++j) n += c[j] >= t ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, n) >= static_cast<unsigned>(k)) res = t;
   }
-  if (warp == 0) {
-    const uint64_t kth = warp_list_get<R>(v, k - 1);
-    if (lane == 0) kth_out[blockIdx.x] = kth;
-  }
+  if (lane == 0) kth_out[q] = static_cast<uint64_t>(res) << 32;
 }
 
 }  // namespace
 
 cudaError_t launch_kth_of_lists(const uint64_t* keys, int queries, int total, int k, uint64_t* kth_out,
                                 cudaStream_t stream) {
-  if (total < 1 || total > kKthMaxKeys || k < 1 || k > RBF_KTH_MAX_K) return cudaErrorInvalidValue;
+  if (queries < 1 || total < 1 || total > RBF_KTH_MAX_KEYS || k < 1 || k > RBF_KTH_MAX_K) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(queries));
-  cfg.blockDim = dim3(kKthWarps * 32);
+  cfg.gridDim = dim3(static_cast<unsigned>((queries + kKthWarpsPerCta - 1) / kKthWarpsPerCta));
+  cfg.blockDim = dim3(kKthWarpsPerCta * 32);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  switch (list_width(k)) {
-    case 32: return cudaLaunchKernelEx(&cfg, kth_of_lists_kernel<32>, keys, total, k, kth_out);
-    case 64: return cudaLaunchKernelEx(&cfg, kth_of_lists_kernel<64>, keys, total, k, kth_out);
-    case 128: return cudaLaunchKernelEx(&cfg, kth_of_lists_kernel<128>, keys, total, k, kth_out);
-    case 256: return cudaLaunchKernelEx(&cfg, kth_of_lists_kernel<256>, keys, total, k, kth_out);
-    default: return cudaErrorInvalidValue;
-  }
+  return cudaLaunchKernelEx(&cfg, kth_code_kernel, keys, queries, total, k, kth_out);
 }
 
 cudaError_t launch_encode_shard_lists(const int32_t* idx, const float* score, int g, int b, int k, int kp,

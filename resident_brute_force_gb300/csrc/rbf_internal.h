@@ -111,9 +111,10 @@ struct MergeLaunch {
 };
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t stream);
 
-// For each of `queries` queries, the K-th largest of its `total` keys (stored
-// contiguously per query; distinct except for empty zero keys) into
-// kth_out[query], or 0 if fewer than K are nonzero. total <= 1024, K <= 256.
+// For each of `queries` queries, a lower bound on the K-th largest of its
+// `total` keys (stored contiguously per query; keys of distinct rows, zero for
+// none) into kth_out[query]: c << 32, c the largest score code that K of the
+// keys reach; 0 if fewer than K are nonzero. total <= 1024, K <= 256.
 constexpr int RBF_KTH_MAX_KEYS = 1024;
 constexpr int RBF_KTH_MAX_K = 256;
 cudaError_t launch_kth_of_lists(const uint64_t* keys, int queries, int total, int k, uint64_t* kth_out,
