@@ -146,21 +146,24 @@ __global__ void encode_shard_lists_kernel(const int32_t* __restrict__ idx, const
 // such warps without shared memory fits beside a scoring CTA on its SM, and
 // 128 of them cover 256 queries, one per SM beside the pre-pass: the main
 // pass's CTAs never wait for these to leave.
-constexpr int kKthPerLane = RBF_KTH_MAX_KEYS / 32;
+// PL keys per lane (PL * 32 >= total); the per-bit count runs in four
+// independent sums so that it is not one long chain of dependent adds.
 constexpr int kKthWarpsPerCta = 2;
 
+template <int PL>
 __global__ void __launch_bounds__(kKthWarpsPerCta * 32) kth_code_kernel(const uint64_t* __restrict__ keys,
                                                                         int queries, int total, int k,
                                                                         uint64_t* __restrict__ kth_out) {
+  static_assert(PL % 4 == 0 && PL * 32 <= RBF_KTH_MAX_KEYS, "keys per lane");
   pdl_launch_dependents();  // the main pass may be scheduled now; it waits for the bounds
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int q = blockIdx.x * kKthWarpsPerCta + (threadIdx.x >> 5);
   if (q >= queries) return;
   const uint64_t* src = keys + static_cast<size_t>(q) * total;
-  uint32_t c[kKthPerLane];
+  uint32_t c[PL];
 #pragma unroll
-  for (int j = 0; j < kKthPerLane; ++j) {
+  for (int j = 0; j < PL; ++j) {
     const int i = j * 32 + lane;
     c[j] = i < total ? static_cast<uint32_t>(__ldcg(src + i) >> 32) : 0u;
   }
@@ -168,10 +171,10 @@ __global__ void __launch_bounds__(kKthWarpsPerCta * 32) kth_code_kernel(const ui
 #pragma unroll 1
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t t = res | (1u << bit);
-    unsigned n = 0;
+    unsigned n[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int j = 0; j < kKthPerLane; ++j) n += c[j] >= t ? 1u : 0u;
-    if (__reduce_add_sync(0xffffffffu, n) >= static_cast<unsigned>(k)) res = t;
+    for (int j = 0; j < PL; ++j) n[j & 3] += c[j] >= t ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, (n[0] + n[1]) + (n[2] + n[3])) >= static_cast<unsigned>(k)) res = t;
   }
   if (lane == 0) kth_out[q] = static_cast<uint64_t>(res) << 32;
 }
@@ -190,7 +193,11 @@ cudaError_t launch_kth_of_lists(const uint64_t* keys, int queries, int total, in
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kth_code_kernel, keys, queries, total, k, kth_out);
+  const int per_lane = (total + 31) / 32;
+  if (per_lane <= 8) return cudaLaunchKernelEx(&cfg, kth_code_kernel<8>, keys, queries, total, k, kth_out);
+  if (per_lane <= 16) return cudaLaunchKernelEx(&cfg, kth_code_kernel<16>, keys, queries, total, k, kth_out);
+  if (per_lane <= 24) return cudaLaunchKernelEx(&cfg, kth_code_kernel<24>, keys, queries, total, k, kth_out);
+  return cudaLaunchKernelEx(&cfg, kth_code_kernel<32>, keys, queries, total, k, kth_out);
 }
 
 cudaError_t launch_encode_shard_lists(const int32_t* idx, const float* score, int g, int b, int k, int kp,
