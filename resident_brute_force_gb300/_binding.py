@@ -187,7 +187,11 @@ def _any_ptr(x, np_dtype, torch_dtype_name: str) -> tuple[object, int]:
 
 
 class Engine:
-    """An engine with every buffer preallocated (see ``rbf_create``)."""
+    """An engine with every buffer preallocated (see ``rbf_create``).
+
+    Like the handle it wraps, one Engine serves one call at a time (its
+    host-buffer calls also share small host arrays); concurrent callers each
+    take their own ``view()``."""
 
     def __init__(self, max_n: int, max_d: int, max_k: int = RBF_MAX_K, max_batch: int = 1,
                  flags: int = 0, stream=None, _view_of=None):
