@@ -79,10 +79,17 @@ typedef enum rbf_option {
   RBF_OPT_SMEM_BUDGET = 3,   /* shared-memory ring budget per CTA, bytes */
   RBF_OPT_TIMEOUT_NS = 4,    /* bound on every device-side wait (default 2e9) */
   RBF_OPT_SCHEDULE = 5,      /* 0 = static row ranges, 1 = dynamic tile claims (default) */
-  RBF_OPT_BATCH_SAMPLE = 6   /* rows of the batched path's bound pre-pass: -1 = automatic
-                                (default: 16,384 per 32 of K, at most N/4, none below 16,384),
-                                0 = no pre-pass, else that many leading rows (a multiple of 256,
-                                at most N). Changes speed only, never results. */
+  RBF_OPT_BATCH_SAMPLE = 6,  /* rows of the batched path's bound pre-pass: -1 = automatic
+                                (default: 16,384 per 32 of K, at most N/4 and none below
+                                N = 65,536, rounded up to whole rounds of 256-row tiles over
+                                every CTA pair), 0 = no pre-pass, else that many leading rows (a
+                                multiple of 256, at most N). Changes speed only, never results. */
+  RBF_OPT_HOST_READ = 7      /* 1 = search_resident_batch's first kernel reads the caller's
+                                query buffer in place (the default where the device reads pageable
+                                host memory through the host's page tables, as a GB300 with its
+                                Grace host does over NVLink-C2C; UNSUPPORTED elsewhere); 0 = the
+                                queries are first copied into the engine's pinned staging block.
+                                Changes speed only, never results. */
 } rbf_option;
 
 /* ------------------------------------------------------------------ engine */

@@ -35,6 +35,7 @@ RBF_OPT_SMEM_BUDGET = 3
 RBF_OPT_TIMEOUT_NS = 4
 RBF_OPT_SCHEDULE = 5
 RBF_OPT_BATCH_SAMPLE = 6
+RBF_OPT_HOST_READ = 7
 
 FAULT_COPY = 1
 FAULT_LAUNCH = 2

@@ -69,6 +69,8 @@ struct rbf_engine {
   uint64_t* theta0 = nullptr;    // per query: K-th key over the row sample
   int* lens = nullptr;           // batched K > 32: keys in each per-CTA list of a 256-query group
   int64_t batch_sample = -1;     // RBF_OPT_BATCH_SAMPLE
+  int host_read = 0;             // RBF_OPT_HOST_READ: kernels may read the caller's pageable host buffers
+  int host_read_ok = 0;          // the device reads pageable host memory through the host's page tables
   int max_pitch_bf16 = 0;
   int pitch_bf16 = 0;
   int query_rows = 0;            // max_batch rounded up to 256
@@ -471,6 +473,15 @@ rbf_status rbf_create(int64_t max_n, int32_t max_d, int32_t max_k, int32_t max_b
   }
   cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, e->device);
   cudaDeviceGetAttribute(&e->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, e->device);
+  {
+    // Address translation through the host's page tables (GB300's Grace
+    // host over NVLink-C2C): a kernel may read any host buffer in place.
+    int pageable = 0, host_tables = 0;
+    cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, e->device);
+    cudaDeviceGetAttribute(&host_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables, e->device);
+    e->host_read_ok = pageable && host_tables ? 1 : 0;
+    e->host_read = e->host_read_ok;
+  }
   e->max_n = max_n;
   e->max_d = max_d;
   e->max_k = max_k;
@@ -547,6 +558,8 @@ rbf_status rbf_create_view(rbf_engine* base, void* cuda_stream, rbf_engine** out
   e->timeout_ns = base->timeout_ns;
   e->dynamic = base->dynamic;
   e->batch_sample = base->batch_sample;
+  e->host_read = base->host_read;
+  e->host_read_ok = base->host_read_ok;
   e->owner = base;
   e->seen_version = base->corpus_version - 1;  // read the corpus state at the first call
   try {
@@ -622,6 +635,11 @@ rbf_status rbf_set_option(rbf_engine* e, rbf_option opt, int64_t value) {
     case RBF_OPT_BATCH_SAMPLE:
       if (value < -1 || (value > 0 && value % 256 != 0)) return RBF_ERR_INVALID_VALUE;
       e->batch_sample = value;
+      return RBF_OK;
+    case RBF_OPT_HOST_READ:
+      if (value < 0 || value > 1) return RBF_ERR_INVALID_VALUE;
+      if (value == 1 && !e->host_read_ok) return RBF_ERR_UNSUPPORTED;
+      e->host_read = static_cast<int>(value);
       return RBF_OK;
   }
   return RBF_ERR_INVALID_VALUE;
@@ -969,14 +987,21 @@ rbf_status search_resident_batch(rbf_engine* e, const float* queries, int32_t b,
   if (rbf_status s = check_k(e, k)) return s;
   const size_t qbytes = static_cast<size_t>(b) * e->d * 4;
   e->launches = 0;
-  // The queries go to the device through the pinned staging block, which the
-  // query conversion kernel reads in place (mapped; coherent over NVLink-C2C
-  // on GB300), as the single-query search does: that is the call's copy.
+  // The query conversion kernel reads the queries on the host (coherent over
+  // NVLink-C2C on GB300): where the device reads pageable memory through the
+  // host's page tables, straight from the caller's buffer (the call is
+  // synchronous, so the buffer outlives every read); else from the pinned
+  // staging block they are first copied into, as the single-query search
+  // does. Either way that is the call's host-to-device transfer.
   if (inject(e, 1)) return RBF_ERR_CUDA;
-  std::memcpy(e->h_query, queries, qbytes);
+  const float* src = queries;
+  if (!e->host_read) {
+    std::memcpy(e->h_query, queries, qbytes);
+    src = e->d_hquery;
+  }
   const size_t count = static_cast<size_t>(b) * k;
   const ResultLayout L = result_layout(count, 4);
-  if (rbf_status s = enqueue_batch(e, e->d_hquery, b, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
+  if (rbf_status s = enqueue_batch(e, src, b, k, reinterpret_cast<int32_t*>(e->d_hres + L.a_off),
                                    reinterpret_cast<float*>(e->d_hres + L.b_off), reinterpret_cast<int*>(e->d_hres)))
     return s;
   if (rbf_status s = finish_host_call(e, L)) return s;

@@ -91,6 +91,38 @@ def test_dev_matches_host_and_repeats(rbf):
         assert e.check_device_error() == rbf.RBF_OK
 
 
+@pytest.mark.parametrize("flags", ["bf16", "tf32", "cosine"])
+def test_host_read_in_place_matches_staging(rbf, flags):
+    """search_resident_batch reads the caller's query buffer in place where the
+    device reads pageable host memory through the host's page tables
+    (RBF_OPT_HOST_READ = 1, the default there) and through the pinned staging
+    block otherwise (0): the results are identical, and exact on dyadic data.
+    The queries are a strided view copied to a fresh buffer by the binding,
+    and a plain numpy array, so both fresh and long-lived pages are read."""
+    n, d, b, k = 20_011, 96, 37, 16
+    c = workloads.dyadic_grid(n, d, seed=13)
+    qs = workloads.dyadic_grid(2 * b, d, seed=14)[::2]
+    f = {"bf16": rbf.RBF_FLAG_BF16_CORPUS, "tf32": 0, "cosine": rbf.RBF_FLAG_BF16_CORPUS | rbf.RBF_FLAG_COSINE}[flags]
+    with rbf.Engine(n, d, k, max_batch=b, flags=f) as e:
+        e.upload_corpus_rowmajor(c)
+        with pytest.raises(rbf.RbfError) as ei:
+            e.set_option(rbf.RBF_OPT_HOST_READ, 2)
+        assert ei.value.status == rbf.RBF_ERR_INVALID_VALUE
+        e.set_option(rbf.RBF_OPT_HOST_READ, 0)
+        ref_idx, ref_sc = e.search_resident_batch(qs, k)
+        try:
+            e.set_option(rbf.RBF_OPT_HOST_READ, 1)
+        except rbf.RbfError as err:
+            assert err.status == rbf.RBF_ERR_UNSUPPORTED
+            pytest.skip("the device does not read pageable host memory")
+        for q in (qs, np.ascontiguousarray(qs)):
+            idx, sc = e.search_resident_batch(q, k)
+            assert np.array_equal(idx, ref_idx) and np.array_equal(sc, ref_sc)
+        if flags == "bf16":
+            for j in range(0, b, 6):
+                check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], k))
+
+
 def test_invalid_and_k_above_32(rbf):
     c = workloads.dyadic_grid(500, 64, seed=21)
     qs = workloads.dyadic_grid(4, 64, seed=22)
