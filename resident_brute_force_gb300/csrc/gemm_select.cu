@@ -790,6 +790,38 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, int64_t src_pitch,
   }
 }
 
+// As to_bf16_kernel, four elements per thread: one 16-byte load and one
+// 8-byte store (src 16-byte aligned, src_pitch and dst_pitch multiples of 4);
+// a row's last partial group of four is read element by element.
+__global__ void to_bf16_x4_kernel(const float* __restrict__ src, int64_t src_pitch, __nv_bfloat16* __restrict__ dst,
+                                  int64_t dst_pitch, int64_t rows, int64_t rows_total, int cols) {
+  pdl_launch_dependents();  // the scoring pass may become resident now; its producer waits for these queries
+  const int64_t total4 = rows_total * dst_pitch / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i * 4;
+    const int64_t r = e / dst_pitch;
+    const int c = static_cast<int>(e - r * dst_pitch);
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (r < rows) {
+      const float* x = src + r * src_pitch + c;
+      if (c + 3 < cols) {
+        v = *reinterpret_cast<const float4*>(x);
+      } else {
+        if (c < cols) v.x = x[0];
+        if (c + 1 < cols) v.y = x[1];
+        if (c + 2 < cols) v.z = x[2];
+      }
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&lo);
+    w.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst + e) = w;
+  }
+}
+
 // fp32 [rows][src_pitch] -> bf16 tile-major [tiles][kchunks][128][64], zero
 // past `cols` and for rows in [rows, tiles * 128).
 __global__ void to_bf16_tiled_kernel(const float* __restrict__ src, int64_t src_pitch,
@@ -867,12 +899,18 @@ bool make_f32_tensor_map(void* map_out, const void* base, int64_t rows, int pitc
 
 cudaError_t launch_to_bf16(const float* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,
                            int64_t rows_total, int cols, int num_sms, cudaStream_t st) {
-  const int64_t total = rows_total * dst_pitch;
+  const bool x4 = (reinterpret_cast<uintptr_t>(src) & 15) == 0 && src_pitch % 4 == 0 && dst_pitch % 4 == 0 &&
+                  (reinterpret_cast<uintptr_t>(dst) & 7) == 0;
+  const int64_t total = rows_total * dst_pitch / (x4 ? 4 : 1);
   int64_t blocks = (total + 255) / 256;
   blocks = blocks < int64_t(num_sms) * 8 ? blocks : int64_t(num_sms) * 8;
   if (blocks < 1) blocks = 1;
-  to_bf16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, static_cast<__nv_bfloat16*>(dst),
-                                                          dst_pitch, rows, rows_total, cols);
+  if (x4)
+    to_bf16_x4_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, static_cast<__nv_bfloat16*>(dst),
+                                                               dst_pitch, rows, rows_total, cols);
+  else
+    to_bf16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(src, src_pitch, static_cast<__nv_bfloat16*>(dst),
+                                                            dst_pitch, rows, rows_total, cols);
   return cudaGetLastError();
 }
 
