@@ -992,10 +992,16 @@ def main(argv=None):
         rbf._build.build()
     if sharded:
         line = run_sharded(rbf, args, rank, world)
-        if rank == 0:
-            print(json.dumps(line), flush=True)
         import torch.distributed as dist
         dist.destroy_process_group()
+        # NCCL may print to stdout through C stdio (buffered until exit): flush
+        # it first so that the result is the last line.
+        try:
+            ctypes.CDLL(None).fflush(None)
+        except Exception:
+            pass
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         return 0
 
     clocks = ClockSampler(local).start()
