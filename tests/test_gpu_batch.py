@@ -123,6 +123,37 @@ def test_host_read_in_place_matches_staging(rbf, flags):
                 check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], k))
 
 
+def test_unaligned_query_buffers(rbf):
+    """Query buffers that start 4 bytes past a 16-byte boundary (host and
+    device) take the element-wise conversion path; the results equal those of
+    aligned buffers, and D not a multiple of 4 leaves a partial group per row."""
+    import torch
+    for d in (96, 98):
+        n, b, k = 9_001, 19, 8
+        c = workloads.dyadic_grid(n, d, seed=15)
+        qs = workloads.dyadic_grid(b, d, seed=16)
+        raw = np.zeros(b * d + 8, dtype=np.float32)
+        base = (-raw.ctypes.data // 4) % 4  # first 16-byte aligned element
+        off = np.ndarray((b, d), dtype=np.float32, buffer=raw, offset=4 * (base + 1))
+        off[...] = qs
+        assert off.ctypes.data % 16 == 4
+        with engine(rbf, n, d, b, k) as e:
+            e.upload_corpus_rowmajor(c)
+            ref_idx, ref_sc = e.search_resident_batch(np.ascontiguousarray(qs), k)
+            idx, sc = e.search_resident_batch(off, k)
+            assert np.array_equal(idx, ref_idx) and np.array_equal(sc, ref_sc)
+            flat = torch.zeros(b * d + 1, dtype=torch.float32, device="cuda")
+            dq = flat[1:].view(b, d)
+            dq.copy_(torch.from_numpy(qs))
+            di = torch.empty((b, k), dtype=torch.int32, device="cuda")
+            ds = torch.empty((b, k), dtype=torch.float32, device="cuda")
+            e.search_resident_batch_dev(dq, k, di, ds)
+            torch.cuda.synchronize()
+            assert np.array_equal(di.cpu().numpy(), ref_idx) and np.array_equal(ds.cpu().numpy(), ref_sc)
+            for j in range(0, b, 6):
+                check_exact(idx[j], sc[j], *oracle.topk(c, qs[j], k))
+
+
 def test_invalid_and_k_above_32(rbf):
     c = workloads.dyadic_grid(500, 64, seed=21)
     qs = workloads.dyadic_grid(4, 64, seed=22)
