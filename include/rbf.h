@@ -242,6 +242,12 @@ rbf_status merge_partial_topk_dev(rbf_engine* engine, int32_t k, int32_t* d_idx,
  *              preallocated partials buffer, 256 queries at a time.
  *   out_idx    host, B x K int32 (row q holds query q's list, best-first)
  *   out_score  host, B x K fp32
+ * The call is synchronous. Where the device reads pageable host memory
+ * through the host's page tables (RBF_OPT_HOST_READ, on by default there) its
+ * first kernel reads `queries` in place, so the buffer must be ordinary host
+ * memory the process can read; otherwise the queries are copied into the
+ * engine's pinned staging block first. The outputs are written only on
+ * success.
  * Errors: INVALID_VALUE, NOT_READY, CUDA, TIMEOUT. */
 rbf_status search_resident_batch(rbf_engine* engine, const float* queries, int32_t b, int32_t k,
                                  int32_t* out_idx, float* out_score);
